@@ -1,0 +1,149 @@
+"""Seeded synthetic inputs for the KPool indexer.
+
+This module draws random numbers and nothing else: it holds none of the
+method's arithmetic, so the CUDA path and the CPU oracle can both take their
+inputs from it.  Draw order and distributions (seed 0 by default, a
+``torch.Generator``):
+
+1. document lengths (packed-THD workloads only): ``u_i ~ U[lo, hi)`` in
+   float64, ``L_i = floor(u_i * T / sum(u))``, the remainder added to the
+   last document;
+2. ``q [T, H, D]``, 3. ``k [T, D]``, 4. ``gate [T, D]``: N(0, 1) drawn in
+   float32 and rounded to bfloat16 by torch;
+5. ``ape [kpool, D]``: N(0, 0.1^2) float32;
+6. ``w [T, H]``: N(0, 1) / sqrt(H) float32.
+
+Large tensors are drawn in row chunks of ``CHUNK_ELEMS`` elements so that the
+float32 staging buffer stays small; the chunking is part of the definition.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+CHUNK_ELEMS = 1 << 26
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    H: int
+    D: int
+    kpool: int
+    index_topk: int
+    tail: bool = True
+    n_docs: int = 1
+    doc_len_range: tuple | None = None   # (lo, hi) for seeded packed-THD lengths
+    equal_docs: bool = False              # batch of equal sequences
+    fp8: bool = False
+    seed: int = 0
+    desc: str = ""
+
+    @property
+    def Kp(self) -> int:
+        return self.index_topk // self.kpool
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", T=256, H=4, D=32, kpool=4, index_topk=32,
+                     desc="Tiny single sequence T=256 H=4 D=32 kpool=4 index_topk=32"),
+    "single_8k": Workload("single_8k", T=8192, H=64, D=128, kpool=4, index_topk=2048,
+                          desc="Single sequence T=8192 H=64 D=128 kpool=4 index_topk=2048"),
+    "thd_32k": Workload("thd_32k", T=32768, H=64, D=128, kpool=4, index_topk=2048,
+                        n_docs=16, doc_len_range=(256, 4096),
+                        desc="Packed THD: 16 documents, lengths U[256,4096] rescaled to "
+                             "32768 tokens, H=64 D=128 kpool=4 index_topk=2048"),
+    "long_128k": Workload("long_128k", T=131072, H=64, D=128, kpool=4, index_topk=2048,
+                          desc="Long single sequence T=131072 H=64 D=128 kpool=4 "
+                               "index_topk=2048"),
+    "fp8_2x32k": Workload("fp8_2x32k", T=65536, H=64, D=128, kpool=4, index_topk=2048,
+                          n_docs=2, equal_docs=True, fp8=True,
+                          desc="FP8 indexer mode: 2 sequences of 32768 tokens, H=64 D=128 "
+                               "kpool=4 index_topk=2048, E4M3 scoring"),
+}
+
+
+def doc_lengths(wl: Workload, gen: torch.Generator) -> list:
+    if wl.n_docs == 1:
+        return [wl.T]
+    if wl.equal_docs:
+        assert wl.T % wl.n_docs == 0
+        return [wl.T // wl.n_docs] * wl.n_docs
+    lo, hi = wl.doc_len_range
+    u = torch.rand(wl.n_docs, generator=gen, dtype=torch.float64) * (hi - lo) + lo
+    lens = [int(math.floor(float(x) * wl.T / float(u.sum()))) for x in u]
+    lens[-1] += wl.T - sum(lens)
+    return lens
+
+
+def _normal_bf16(shape, gen, scale=1.0):
+    n = 1
+    for s in shape:
+        n *= s
+    out = torch.empty(n, dtype=torch.bfloat16)
+    pos = 0
+    while pos < n:
+        m = min(CHUNK_ELEMS, n - pos)
+        x = torch.randn(m, generator=gen, dtype=torch.float32)
+        if scale != 1.0:
+            x *= scale
+        out[pos:pos + m] = x.to(torch.bfloat16)
+        pos += m
+    return out.view(*shape)
+
+
+@dataclass
+class Inputs:
+    wl: Workload
+    cu_seqlens: torch.Tensor      # int32 [n_docs + 1]
+    q: torch.Tensor               # bf16 [T, H, D]
+    k: torch.Tensor               # bf16 [T, D]
+    gate: torch.Tensor            # bf16 [T, D]
+    ape: torch.Tensor             # fp32 [kpool, D]
+    w: torch.Tensor               # fp32 [T, H]
+    extra: dict = field(default_factory=dict)
+
+
+def make_inputs(wl: Workload, seed: int | None = None, T: int | None = None) -> Inputs:
+    """Draw the inputs of workload ``wl`` on the CPU.  ``T`` overrides the
+    token count (same recipe, used for reduced-size parity cases)."""
+    if T is not None and T != wl.T:
+        from dataclasses import replace
+        wl = replace(wl, T=T)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(wl.seed if seed is None else seed)
+    lens = doc_lengths(wl, gen)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    cu_seqlens = torch.tensor(cu, dtype=torch.int32)
+    q = _normal_bf16((wl.T, wl.H, wl.D), gen)
+    k = _normal_bf16((wl.T, wl.D), gen)
+    gate = _normal_bf16((wl.T, wl.D), gen)
+    ape = torch.randn(wl.kpool, wl.D, generator=gen, dtype=torch.float32) * 0.1
+    w = torch.randn(wl.T, wl.H, generator=gen, dtype=torch.float32) / math.sqrt(wl.H)
+    return Inputs(wl, cu_seqlens, q, k, gate, ape, w)
+
+
+def sample_rows(T: int, n_sample: int = 1024, edge: int = 64, seed: int = 0,
+                lo: int = 0, hi: int | None = None) -> torch.Tensor:
+    """Rows checked at full size: ``n_sample`` rows drawn without replacement
+    from [lo+edge, hi-edge) plus the first and last ``edge`` rows of
+    [lo, hi).  Sorted, int64."""
+    hi = T if hi is None else hi
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    inner = hi - lo - 2 * edge
+    if inner <= n_sample:
+        return torch.arange(lo, hi, dtype=torch.int64)
+    pick = torch.randperm(inner, generator=gen)[:n_sample] + lo + edge
+    rows = torch.cat([torch.arange(lo, lo + edge), pick, torch.arange(hi - edge, hi)])
+    return torch.sort(rows.to(torch.int64)).values
+
+
+def bits(t: torch.Tensor):
+    """bf16 tensor -> numpy uint16 bit patterns (a view, no arithmetic)."""
+    return t.contiguous().view(torch.int16).numpy().view("uint16")
