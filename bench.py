@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Benchmark of the KPool DSA indexer hot path on GB300.
+
+One step = the whole path over one batch of synthetic input:
+  kpool_compress -> [kpool_quantize_fp8 (FP8 mode)] -> kpool_score_topk ->
+  kpool_expand_indices
+on the default workload ``long_128k`` (one sequence of T = 131072 tokens,
+H = 64, D = 128, kpool = 4, index_topk = 2048), the size the scoring
+kernel's tensor-core target is stated at.
+
+Prints ONE JSON line (rank 0).  ``value`` is whole-job queries/s with inputs
+resident in HBM; ``e2e`` is the same metric through the public API with the
+inputs copied from pinned host memory and the token indices read back every
+step; ``roofline`` is the dominant kernel (kpool_score_topk) against the
+measured dense BF16 tensor peak; ``cpu_baseline`` is the CPU oracle timed on
+a bounded sample of query rows of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle arm
+Under torchrun (N > 1) every rank runs an independent replica (the path has
+no exchange step); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_kpool_compress_gb300 import workloads as W  # noqa: E402
+
+METRIC = "KPool indexer queries/s and scoring TFLOP/s (% of GB300 BF16/FP8 peak)"
+UNIT = "queries/s"
+SCORE_SRC = os.path.join(ROOT, "sparse_attention_kpool_compress_gb300", "csrc", "kpool_score.cu")
+
+
+def sum_floor(L, kp):
+    """sum_{x=1}^{L} floor(x / kp)."""
+    m = L // kp
+    return kp * m * (m - 1) // 2 + m * (L - m * kp + 1)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def file_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """Per-launch DRAM bytes from a committed ncu summary, or None if absent or
+    taken on a different version of the kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get("%s/%s" % (kernel, workload))
+    if not e or e.get("source_sha256_16") != file_hash(SCORE_SRC):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline leg and the reference arm only)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(inp, rows, n_threads=None):
+    """Time the oracle as it stands on the given query rows: compression of
+    every pool, selection for the rows, expansion of the rows."""
+    import oracle as ora
+    ora.build()
+    wl = inp.wl
+    cu = inp.cu_seqlens.numpy() if inp.cu_seqlens.numel() > 2 else None
+    kb, gb, qb = W.bits(inp.k), W.bits(inp.gate), W.bits(inp.q)
+    t0 = time.perf_counter()
+    pk = ora.compress(kb, gb, inp.ape.numpy(), cu, wl.kpool)
+    if wl.fp8:
+        qc, qs = ora.fp8_rows(qb[rows].reshape(-1, 128))
+        pc, ps = ora.fp8_rows(pk)
+        # score only the sampled rows: place their codes at their token rows
+        qfull = np.zeros((wl.T, wl.H, 128), np.uint8)
+        qsf = np.ones((wl.T, wl.H), np.float32)
+        qfull[rows] = qc.reshape(len(rows), wl.H, 128)
+        qsf[rows] = qs.reshape(len(rows), wl.H)
+        ops = ora.Operands(qfull, inp.w.numpy(), pc, qsf, ps)
+    else:
+        ops = ora.Operands(qb, inp.w.numpy(), pk)
+    o = ora.select_rows(ops, cu, wl.kpool, wl.Kp, rows)
+    ora.expand_rows(o["sel"], cu, wl.T, wl.kpool, wl.Kp, wl.tail, rows)
+    dt = time.perf_counter() - t0
+    return dt, ora.num_threads()
+
+
+def baseline_rows(wl, n, seed=1):
+    g = torch.Generator().manual_seed(seed)
+    return torch.sort(torch.randperm(wl.T, generator=g)[:n]).values.numpy().astype(np.int64)
+
+
+# ---------------------------------------------------------------------------
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = W.make_inputs(wl)
+    rows = baseline_rows(wl, args.ref_rows)
+    for _ in range(args.warmup):
+        oracle_sample(inp, rows[: max(1, len(rows) // 8)])
+    times = []
+    cores = 1
+    for _ in range(args.steps):
+        dt, cores = oracle_sample(inp, rows)
+        times.append(dt)
+    ms = 1000.0 * sum(times) / len(times)
+    value = len(rows) / (ms / 1000.0)
+    sample = ("%d uniformly drawn query rows of %s per step (compression of all %d pools, "
+              "selection and expansion of the rows)" % (len(rows), wl.name, wl.T // wl.kpool))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "desc": wl.desc, "T": wl.T, "H": wl.H, "D": wl.D,
+                   "kpool": wl.kpool, "index_topk": wl.index_topk, "fp8": wl.fp8},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_128k", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--baseline-rows", type=int, default=96)
+    ap.add_argument("--ref-rows", type=int, default=48)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warmup raised to 3 (minimum)", file=sys.stderr)
+        args.warmup = 3
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import sparse_attention_kpool_compress_gb300 as K
+
+    dev = torch.device("cuda", local)
+    inp = W.make_inputs(wl)
+    T, H, D, kp, topk, Kp = wl.T, wl.H, wl.D, wl.kpool, wl.index_topk, wl.Kp
+    multi = inp.cu_seqlens.numel() > 2
+    if multi:
+        cu_pools_h, P = K.kpool_num_pools(inp.cu_seqlens, T, kp)
+        cu = inp.cu_seqlens.to(dev)
+        cp = cu_pools_h.to(dev)
+        n_docs = inp.cu_seqlens.numel() - 1
+    else:
+        P, cu, cp, n_docs = T // kp, None, None, 1
+
+    q = inp.q.to(dev)
+    k = inp.k.to(dev)
+    gate = inp.gate.to(dev)
+    ape = inp.ape.to(dev)
+    w = inp.w.to(dev)
+    pk = torch.empty(P, D, dtype=torch.bfloat16, device=dev)
+    pool_idx = torch.empty(T, Kp, dtype=torch.int32, device=dev)
+    pool_score = torch.empty(T, Kp, dtype=torch.float32, device=dev)
+    Wd = Kp * kp + kp - 1
+    tok = torch.empty(T, Wd, dtype=torch.int32, device=dev)
+    ws = K.new_workspace(T, H, n_docs, dev)
+    if wl.fp8:
+        pk8 = torch.empty(P, D, dtype=torch.uint8, device=dev)
+        pks = torch.empty(P, dtype=torch.float32, device=dev)
+        q8 = torch.empty(T, H, D, dtype=torch.uint8, device=dev)
+        qs = torch.empty(T, H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    B = K.binding
+    L = B._lib
+    sp = B._stream(dev)
+
+    def chk(rc, name):
+        if rc != 0:
+            raise B.KPoolError(rc, name)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if wl.fp8:
+            chk(L.kpool_compress(B._ptr(k), B._ptr(gate), B._ptr(ape), B._ptr(cu), B._ptr(cp),
+                                 n_docs, T, D, kp, P, B._ptr(pk), B._ptr(pk8), B._ptr(pks), sp),
+                "kpool_compress")
+            chk(L.kpool_quantize_fp8(B._ptr(q), T * H, D, B._ptr(q8), B._ptr(qs), sp),
+                "kpool_quantize_fp8")
+        else:
+            chk(L.kpool_compress(B._ptr(k), B._ptr(gate), B._ptr(ape), B._ptr(cu), B._ptr(cp),
+                                 n_docs, T, D, kp, P, B._ptr(pk), None, None, sp),
+                "kpool_compress")
+        if ev is not None:
+            ev[1].record(stream)
+        if wl.fp8:
+            chk(L.kpool_score_topk(B._ptr(q8), B._ptr(qs), B._ptr(w), B._ptr(pk8), B._ptr(pks),
+                                   B._ptr(cu), B._ptr(cp), n_docs, T, P, H, D, kp, topk, 1,
+                                   B._ptr(pool_idx), B._ptr(pool_score), B._ptr(ws), ws.numel(),
+                                   sp), "kpool_score_topk")
+        else:
+            chk(L.kpool_score_topk(B._ptr(q), None, B._ptr(w), B._ptr(pk), None, B._ptr(cu),
+                                   B._ptr(cp), n_docs, T, P, H, D, kp, topk, 0, B._ptr(pool_idx),
+                                   B._ptr(pool_score), B._ptr(ws), ws.numel(), sp),
+                "kpool_score_topk")
+        if ev is not None:
+            ev[2].record(stream)
+        chk(L.kpool_expand_indices(B._ptr(pool_idx), B._ptr(cu), B._ptr(cp), n_docs, T, kp, topk,
+                                   int(wl.tail), B._ptr(tok), sp), "kpool_expand_indices")
+        if ev is not None:
+            ev[3].record(stream)
+
+    launches_per_step = 1 + (1 if wl.fp8 else 0) + 2 + 1
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = K.kpool_read_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %d after warm-up" % status)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms_total = e0.elapsed_time(e1)
+    ms_step = ms_total / args.steps
+    t_compress = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_score = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_expand = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    status = K.kpool_read_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %d after the timed steps" % status)
+
+    # ---- end to end through the public API from pinned host memory --------
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hg, ha, hw = (x.pin_memory() for x in (inp.q, inp.k, inp.gate, inp.ape, inp.w))
+        htok = torch.empty(T, Wd, dtype=torch.int32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hg, ha, hw))
+        d2h = htok.numel() * htok.element_size()
+        dq, dk, dg, da, dw = (torch.empty_like(x, device=dev) for x in (hq, hk, hg, ha, hw))
+
+        def e2e_step():
+            for d_, h_ in ((dq, hq), (dk, hk), (dg, hg), (da, ha), (dw, hw)):
+                d_.copy_(h_, non_blocking=True)
+            tk, _, _ = K.kpool_indexer_forward(dq, dk, dg, da, dw, kp, topk, wl.tail, cu, cp,
+                                               P if multi else None, fp8=wl.fp8, workspace=ws)
+            htok.copy_(tk, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        n_e2e = max(2, min(args.steps, 5))
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = a0.elapsed_time(a1) / n_e2e
+        if world > 1:
+            tt = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        e2e = {"value": world * T / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
+               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del dq, dk, dg, da, dw, hq
+
+    # ---- roofline of the dominant kernel ---------------------------------
+    peaks, peak_src = load_peaks()
+    pairs = sum_floor_pairs(inp.cu_seqlens, kp)
+    flops = 2.0 * H * D * pairs
+    achieved = flops / (t_score / 1000.0) / 1e12
+    if wl.fp8:
+        peak = peaks.get("fp8_tflops_sustained") or 2.0 * peaks["bf16_tflops_sustained"]
+        peak_note = ("fp8 sustained " + peak_src) if peaks.get("fp8_tflops_sustained") else \
+            "2 x bf16 sustained (nominal fp8/bf16 ratio) " + peak_src
+    else:
+        peak = peaks["bf16_tflops_sustained"]
+        peak_note = "bf16 sustained (%s)" % peak_src
+    roofline = {"bound": "tensor", "kernel": "kpool_score_topk", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": recorded_traffic("kpool_score_topk", wl.name),
+                "peak_source": peak_note,
+                "frac_of_burst": achieved / (peaks["bf16_tflops"] * (2 if wl.fp8 else 1)),
+                "algorithmic_flops_per_launch": flops, "causal_pairs": pairs,
+                "ms_per_launch": t_score}
+    comp_bytes = T * D * 2 * 2 + P * D * 2
+    side = {"compress_ms": t_compress, "compress_gbs": comp_bytes / (t_compress / 1000.0) / 1e9,
+            "compress_frac_hbm": comp_bytes / (t_compress / 1000.0) / 1e9 / peaks["hbm_gbs"],
+            "expand_ms": t_expand,
+            "expand_gbs": (T * Kp * 4 + T * Wd * 4) / (t_expand / 1000.0) / 1e9,
+            "score_topk_ms": t_score, "score_queries_per_s": T / (t_score / 1000.0)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rows = baseline_rows(wl, args.baseline_rows)
+        dt, cores = oracle_sample(inp, rows)
+        cpu = {"value": len(rows) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%d uniformly drawn query rows of %s (compression of all pools, "
+                         "selection and expansion of those rows), %.1f s" % (len(rows), wl.name, dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * T / (ms_step / 1000.0), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8-e4m3" if wl.fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "desc": wl.desc, "T": T, "H": H, "D": D,
+                       "kpool": kp, "index_topk": topk, "tail": wl.tail, "fp8": wl.fp8,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (q alone %.2f GiB)" % (q.numel() * q.element_size() / 2 ** 30)},
+            "scoring_tflops": achieved,
+            "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "kernels": side,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def sum_floor_pairs(cu_seqlens, kp):
+    cs = [int(x) for x in cu_seqlens]
+    return sum(sum_floor(b - a, kp) for a, b in zip(cs[:-1], cs[1:]))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

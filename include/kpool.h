@@ -1,0 +1,218 @@
+/*
+ * kpool.h -- C ABI of the GB300 (sm_103a) KPool DSA indexer library
+ * (libkpool.so).
+ *
+ * The KPool indexer picks, for every query token, the key tokens a sparse
+ * attention layer attends to.  Keys are first compressed kpool tokens at a
+ * time into pooled keys; each query scores the complete pools of its causal
+ * prefix, keeps the best index_topk / kpool pools, and expands them back to
+ * token indices, appending its own incomplete pool (the "tail").  Source:
+ * Megatron-LM PR "GLM5.3 Flash (KDA + mHC + KPool DSA) support + FP8",
+ * Changes section 3 "KPool DSA indexer + NoPE"; SkyRL PR "GLM-5.3-Flash
+ * (glm5_next) Megatron support", commit "k-pool indexer"; xtuner PR
+ * "GLM-5.3-Flash F5: NoPE DSA + KPool indexer", Summary and commit notes.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller unless
+ *    its name ends in _host.  The library never allocates device memory and
+ *    never frees what it is given.
+ *  - Each call enqueues its kernels on `stream` (NULL = legacy default
+ *    stream) and returns without synchronising.  Results are valid once the
+ *    stream has reached that point.
+ *  - Return value: KPOOL_OK (0) or a negative KPOOL_ERR_* code.  All
+ *    argument checks run on the host before anything is enqueued, so a
+ *    rejected call leaves the device untouched.  kpool_last_error() returns
+ *    a message for the last failing call of the calling thread.
+ *  - Layouts are dense row-major.  bf16 tensors are passed as `const void*`
+ *    (raw IEEE bfloat16 bits).  Indices are int32.
+ *  - Document layout ("packed THD"): cu_seqlens[n_docs + 1] holds document
+ *    start offsets into the token axis (cu_seqlens[0] = 0,
+ *    cu_seqlens[n_docs] = T, non-decreasing).  cu_pools[n_docs + 1] holds
+ *    the pool offsets, cu_pools[d+1] - cu_pools[d] = floor(L_d / kpool)
+ *    (kpool_num_pools / kpool_cu_pools compute it).  Pools and causality
+ *    restart at every document start.  Passing cu_seqlens = cu_pools = NULL
+ *    with n_docs = 1 means one sequence of T tokens.
+ *  - Pool p of document d covers tokens cu_seqlens[d] + j*kpool + s,
+ *    s = 0..kpool-1, with j = p - cu_pools[d].  A trailing partial pool of a
+ *    document is not compressed.  A query at document-local position tau
+ *    may select the complete pools j < floor((tau + 1) / kpool).
+ *  - Pool and token indices in outputs are global (packed) indices.
+ */
+#ifndef KPOOL_H_
+#define KPOOL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KPOOL_API __attribute__((visibility("default")))
+#else
+#define KPOOL_API
+#endif
+
+struct CUstream_st;                 /* = cudaStream_t */
+typedef struct CUstream_st *kpool_stream_t;
+
+#define KPOOL_OK 0
+#define KPOOL_ERR_INVALID_ARG (-1)  /* bad pointer, size, alignment or layout */
+#define KPOOL_ERR_UNSUPPORTED (-2)  /* valid but outside the built shapes */
+#define KPOOL_ERR_CUDA (-3)         /* a CUDA runtime/driver call failed */
+#define KPOOL_ERR_WORKSPACE (-4)    /* workspace missing or too small */
+
+/* Device status word bits (kpool_read_status). */
+#define KPOOL_STATUS_TIMEOUT 1      /* a pipeline wait gave up; results invalid */
+#define KPOOL_STATUS_BAD_SEQLENS 2  /* cu_seqlens not 0..T non-decreasing */
+
+/* Message for the last failing call on this host thread ("" if none). */
+KPOOL_API const char *kpool_last_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+KPOOL_API int kpool_version(void);
+
+/*
+ * kpool_num_pools -- host helper: validate a HOST copy of cu_seqlens and
+ * fill cu_pools_host_out[n_docs + 1] (pool offsets, floor(L_d / kpool) pools
+ * per document; Megatron-LM PR section 3: packed THD restarts pools at
+ * document boundaries).  *total_pools_out receives cu_pools[n_docs].
+ * Errors: KPOOL_ERR_INVALID_ARG if cu_seqlens is not 0..T non-decreasing,
+ * kpool < 1, or a pointer is NULL.  Touches no device state.
+ */
+KPOOL_API int kpool_num_pools(const int32_t *cu_seqlens_host, int n_docs, int64_t T, int kpool,
+                    int32_t *cu_pools_host_out, int64_t *total_pools_out);
+
+/*
+ * kpool_cu_pools -- device version of kpool_num_pools: cu_pools_out[n_docs+1]
+ * from device cu_seqlens[n_docs+1].  One small kernel.  No validation of
+ * the device values (see kpool_read_status for the scoring-time check).
+ */
+KPOOL_API int kpool_cu_pools(const int32_t *cu_seqlens, int n_docs, int kpool, int32_t *cu_pools_out,
+                   kpool_stream_t stream);
+
+/*
+ * kpool_compress -- pool compression (Megatron-LM PR section 3; SkyRL
+ * commit "k-pool indexer").  For every complete pool p and dimension d:
+ *     a_s = float(gate[i_s, d]) + ape[s, d]        s = 0..kpool-1
+ *     alpha = softmax_s(a)                          (FP32, max-subtracted)
+ *     pk[p, d] = bf16_rne( sum_s alpha_s * float(k[i_s, d]) )   (FP32 sum)
+ * with i_s the pool's s-th token.
+ *   k, gate      bf16 [T, D], 16-byte aligned
+ *   ape          fp32 [kpool, D]
+ *   cu_seqlens, cu_pools   int32 [n_docs + 1] or both NULL (n_docs = 1)
+ *   P_total      number of pools = cu_pools[n_docs] (T / kpool for one
+ *                sequence); the host must know it to size pk_out
+ *   pk_out       bf16 [P_total, D], 16-byte aligned
+ *   pk_fp8_out, pk_scale_out   NULL, or E4M3 [P_total, D] and fp32
+ *                [P_total]: the FP8 indexer input of the pooled key
+ *                (see kpool_quantize_fp8; requires D = 128)
+ * Supported: D in {32, 64, 128}; 1 <= kpool <= 64.
+ * Errors: INVALID_ARG (NULL/misaligned pointers, bad sizes), UNSUPPORTED.
+ */
+KPOOL_API int kpool_compress(const void *k, const void *gate, const float *ape,
+                   const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs,
+                   int64_t T, int D, int kpool, int64_t P_total, void *pk_out,
+                   uint8_t *pk_fp8_out, float *pk_scale_out, kpool_stream_t stream);
+
+/*
+ * kpool_quantize_fp8 -- FP8 indexer input emulation (Megatron-LM PR
+ * section 3: FP32 Hadamard -> BF16 -> E4M3 with a power-of-two row scale).
+ * For each row r of x (bf16 [rows, 128]):
+ *     y = H128 x / sqrt(128)         FP32, Sylvester-order Hadamard
+ *     b = bf16_rne(y)
+ *     s = smallest power of two with max|b| <= 448 s   (1 for a zero row)
+ *     x_fp8_out[r] = e4m3_rne_satfinite(b / s),  scale_out[r] = s
+ * so that x ~= x_fp8 * s after the rotation.  For q [T, H, 128] pass
+ * rows = T * H.
+ *   x            bf16 [rows, D], 16-byte aligned; D must be 128
+ *   x_fp8_out    uint8 (E4M3) [rows, D]; scale_out fp32 [rows]
+ */
+KPOOL_API int kpool_quantize_fp8(const void *x, int64_t rows, int D, uint8_t *x_fp8_out,
+                       float *scale_out, kpool_stream_t stream);
+
+/*
+ * kpool_score_topk_workspace_size -- bytes of device workspace that
+ * kpool_score_topk / kpool_score_dense need for T tokens, H heads and n_docs
+ * documents (a tile counter, a status word and the query-tile schedule).
+ */
+KPOOL_API size_t kpool_score_topk_workspace_size(int64_t T, int H, int n_docs);
+
+/*
+ * kpool_score_topk -- causal pool scoring fused with top-k selection
+ * (Megatron-LM PR section 3: top-k over index_topk // kpool pools; xtuner
+ * PR: relu homogeneity lets any head_dim^-0.5 factor live in w).
+ *     score[t, p] = sum_h w[t, h] * relu( sum_d q[t, h, d] * pk[p, d] )
+ * over the complete causal pools p of t's document (local index
+ * j < floor((tau+1)/kpool)).  Each row t keeps the Kp = index_topk / kpool
+ * pools of largest score (ties to the lower pool index; every visible pool
+ * when there are at most Kp), written in ascending pool order:
+ *     pool_idx_out[t, 0..Kp)    int32 global pool index, -1 padding
+ *     pool_score_out[t, 0..Kp)  fp32 score, -inf padding
+ * The T x P score matrix is never written to memory.
+ * FP8 mode (fp8 = 1): q and pk are E4M3 codes [T, H, 128] / [P, 128] with
+ * fp32 scales q_scale [T, H] and pk_scale [P] (kpool_quantize_fp8 /
+ * kpool_compress), and
+ *     score = pk_scale[p] * sum_h w[t,h] q_scale[t,h] relu(q_fp8 . pk_fp8)
+ * In bf16 mode q_scale and pk_scale must be NULL.
+ *   q            bf16 [T, H, D] (or E4M3), 16-byte aligned
+ *   w            fp32 [T, H]
+ *   pk           bf16 [P_total, D] (or E4M3), 16-byte aligned
+ *   workspace    >= kpool_score_topk_workspace_size(T, H, n_docs) bytes,
+ *                256-byte aligned; its contents are overwritten.  Calls that
+ *                share one workspace must not overlap on the device.
+ * Supported: H in {4, 8, 16, 32, 64, 128}; D in {32, 64, 128} (128 in FP8
+ * mode); Kp <= a per-H capacity (UNSUPPORTED beyond it).
+ * Device-side: cu_seqlens is validated by the schedule kernel; on failure
+ * or on an internal pipeline timeout the status word (kpool_read_status)
+ * is set and the outputs are not written.
+ */
+KPOOL_API int kpool_score_topk(const void *q, const float *q_scale, const float *w, const void *pk,
+                     const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
+                     int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool,
+                     int index_topk, int fp8, int32_t *pool_idx_out, float *pool_score_out,
+                     void *workspace, size_t workspace_bytes, kpool_stream_t stream);
+
+/*
+ * kpool_score_dense -- test/debug entry: the same scoring as
+ * kpool_score_topk (same kernel pipeline, no selection) written out in full:
+ * scores_out[t, p] (fp32 [T, P_total]) for every complete causal pool p of
+ * t's document, -inf elsewhere.  Meant for small T only.
+ */
+KPOOL_API int kpool_score_dense(const void *q, const float *q_scale, const float *w, const void *pk,
+                      const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
+                      int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool, int fp8,
+                      float *scores_out, void *workspace, size_t workspace_bytes,
+                      kpool_stream_t stream);
+
+/*
+ * kpool_expand_indices -- expansion of selected pools to token indices plus
+ * the causal tail (Megatron-LM PR section 3: fused_qk_topk_kpool expands
+ * pools back to tokens; always_select_tail appends each query's incomplete
+ * causal pool so short prefixes stay fully visible).  Row t of
+ * tok_idx_out [T, W], W = Kp*kpool + kpool - 1:
+ *   for each of the first min(n_c, Kp) entries of pool_idx[t] (ascending
+ *   pools as written by kpool_score_topk) its kpool tokens; then, if
+ *   always_select_tail and r = (tau+1) mod kpool != 0, the r tokens
+ *   t-r+1 .. t; then -1 padding.  Rows are strictly ascending.
+ * An entry of pool_idx outside t's document expands to -1s.
+ */
+KPOOL_API int kpool_expand_indices(const int32_t *pool_idx, const int32_t *cu_seqlens,
+                         const int32_t *cu_pools, int n_docs, int64_t T, int kpool,
+                         int index_topk, int always_select_tail, int32_t *tok_idx_out,
+                         kpool_stream_t stream);
+
+/*
+ * kpool_read_status -- debug helper: synchronously copy the device status
+ * word of a workspace (KPOOL_STATUS_* bits, 0 = clean) to *status_out.
+ * Synchronises the whole device.
+ */
+KPOOL_API int kpool_read_status(const void *workspace, int *status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KPOOL_H_ */

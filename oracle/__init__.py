@@ -72,13 +72,13 @@ def _load():
             "ora_e4m3_from_double": (ctypes.c_uint8, [ctypes.c_double]),
             "ora_pow2_scale": (ctypes.c_double, [ctypes.c_double]),
             "ora_cu_pools": (i64, [P, i32, i32, P]),
-            "ora_compress": (None, [P, P, P, P, i32, i32, i32, P, P]),
+            "ora_compress": (None, [P, P, P, P, i32, i32, i32, P, P, P]),
             "ora_pool_weights": (None, [P, P, i64, i32, i32, P]),
             "ora_hadamard_matrix": (None, [i32, P]),
             "ora_fp8_rows": (None, [P, i64, i32, P, P, P, P]),
-            "ora_score_pairs": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
+            "ora_score_pairs": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i64,
                                        P, P, i64, P, P]),
-            "ora_select_rows": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+            "ora_select_rows": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
                                        P, i64, P, P, P, P, P]),
             "ora_score_rows_full": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                            i64, P, i64, P, P]),
@@ -148,9 +148,11 @@ def cu_pools(cu_seqlens, kp: int) -> np.ndarray:
     return out
 
 
-def compress(k_bits, gate_bits, ape, cu_seqlens, kp: int, want_exact: bool = False):
+def compress(k_bits, gate_bits, ape, cu_seqlens, kp: int, want_exact: bool = False,
+             want_cond: bool = False):
     """k_bits, gate_bits: uint16 bf16 bit patterns [T, D]; ape float32 [kp, D].
-    Returns pk bits uint16 [P_total, D] (and the unrounded doubles)."""
+    Returns pk bits uint16 [P_total, D]; with want_exact also the unrounded
+    doubles, with want_cond also the condition scale sum_s alpha_s |k_s|."""
     k_bits = _c(k_bits, np.uint16)
     gate_bits = _c(gate_bits, np.uint16)
     ape = _c(ape, np.float32)
@@ -158,9 +160,12 @@ def compress(k_bits, gate_bits, ape, cu_seqlens, kp: int, want_exact: bool = Fal
     cs = _seqlens(cu_seqlens, T)
     P = int(cu_pools(cs, kp)[-1])
     pk = np.zeros((P, D), dtype=np.uint16)
-    exact = np.zeros((P, D), dtype=np.float64) if want_exact else None
+    exact = np.zeros((P, D), dtype=np.float64) if (want_exact or want_cond) else None
+    cond = np.zeros((P, D), dtype=np.float64) if want_cond else None
     _load().ora_compress(_ptr(k_bits), _ptr(gate_bits), _ptr(ape), _ptr(cs), len(cs) - 1,
-                         D, kp, _ptr(pk), _ptr(exact))
+                         D, kp, _ptr(pk), _ptr(exact), _ptr(cond))
+    if want_cond:
+        return pk, exact, cond
     return (pk, exact) if want_exact else pk
 
 
@@ -222,7 +227,7 @@ def select_rows(ops: Operands, cu_seqlens, kp: int, Kp: int, rows):
     kth = np.empty(n, dtype=np.float64)
     kth_cond = np.empty(n, dtype=np.float64)
     n_sel = np.empty(n, dtype=np.int32)
-    _load().ora_select_rows(*ops.args(), _ptr(cs), len(cs) - 1, ops.H, ops.D, kp, Kp,
+    _load().ora_select_rows(*ops.args(), _ptr(cs), len(cs) - 1, ops.H, ops.D, kp, ops.P, Kp,
                             _ptr(rows), n, _ptr(sel), _ptr(sel_score), _ptr(kth),
                             _ptr(kth_cond), _ptr(n_sel))
     return dict(sel=sel, sel_score=sel_score, kth=kth, kth_cond=kth_cond, n_sel=n_sel)
@@ -235,7 +240,7 @@ def score_pairs(ops: Operands, cu_seqlens, kp: int, rows, pools):
     n = len(rows)
     sc = np.empty(n, dtype=np.float64)
     cd = np.empty(n, dtype=np.float64)
-    _load().ora_score_pairs(*ops.args(), _ptr(cs), len(cs) - 1, ops.H, ops.D, kp,
+    _load().ora_score_pairs(*ops.args(), _ptr(cs), len(cs) - 1, ops.H, ops.D, kp, ops.P,
                             _ptr(rows), _ptr(pools), n, _ptr(sc), _ptr(cd))
     return sc, cd
 

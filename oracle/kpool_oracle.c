@@ -183,10 +183,11 @@ static int doc_of_token(const int32_t *cu_seqlens, int n_docs, int64_t t)
  *   alpha = softmax over s of a_s
  *   pk    = bf16_rne( sum_s alpha_s * k[i_s, d] )
  * with i_s = doc_start + j*kp + s, in double, rounded once.
- * pk_exact (optional) receives the unrounded double value. */
+ * pk_exact (optional) receives the unrounded double value; pk_cond
+ * (optional) the condition scale sum_s alpha_s * |k[i_s, d]| of the sum. */
 void ora_compress(const uint16_t *k, const uint16_t *gate, const float *ape,
                   const int32_t *cu_seqlens, int n_docs, int D, int kp,
-                  uint16_t *pk_out, double *pk_exact)
+                  uint16_t *pk_out, double *pk_exact, double *pk_cond)
 {
     int32_t *cu_pools = (int32_t *)malloc(sizeof(int32_t) * (n_docs + 1));
     ora_cu_pools(cu_seqlens, n_docs, kp, cu_pools);
@@ -205,15 +206,17 @@ void ora_compress(const uint16_t *k, const uint16_t *gate, const float *ape,
                 }
                 double z = 0.0;
                 for (int s = 0; s < kp; s++) z += exp(a[s] - m);
-                double acc = 0.0;
+                double acc = 0.0, cond = 0.0;
                 for (int s = 0; s < kp; s++) {
                     int64_t i = start + j * kp + s;
                     double alpha = exp(a[s] - m) / z;
                     acc += alpha * ora_bf16_to_double(k[i * D + d]);
+                    cond += alpha * fabs(ora_bf16_to_double(k[i * D + d]));
                 }
                 int64_t g = cu_pools[doc] + j;
                 pk_out[g * D + d] = ora_bf16_from_double(acc);
                 if (pk_exact) pk_exact[g * D + d] = acc;
+                if (pk_cond) pk_cond[g * D + d] = cond;
             }
         }
     }
@@ -309,7 +312,8 @@ void ora_fp8_rows(const uint16_t *x, int64_t rows, int D, uint8_t *codes, float 
 /* ------------------------------------------------------------------ */
 
 /* Operands: either bf16 (qs == NULL) or E4M3 codes with per-row scales.
- * q is [T, H, D]; pk is [P, D]. */
+ * q is [T, H, D]; pk is [P, D].  Values are decoded to double once (exact:
+ * bf16 -> double, and e4m3 * power-of-two scale -> double). */
 typedef struct {
     const void *q;       /* uint16 bf16 or uint8 e4m3 */
     const float *qs;     /* [T, H] scales, NULL for bf16 */
@@ -318,6 +322,8 @@ typedef struct {
     const float *pks;    /* [P] scales, NULL for bf16 */
     int fp8;
     int H, D;
+    int64_t P;
+    double *pkd;         /* decoded pooled keys [P, D] */
 } ora_operands;
 
 static double q_elem(const ora_operands *o, int64_t t, int h, int d)
@@ -334,15 +340,37 @@ static double pk_elem(const ora_operands *o, int64_t p, int d)
     return ora_e4m3_to_double(((const uint8_t *)o->pk)[i]) * (double)o->pks[p];
 }
 
+static void ops_init(ora_operands *o, const void *q, const float *qs, const float *w,
+                     const void *pk, const float *pks, int fp8, int H, int D, int64_t P)
+{
+    o->q = q; o->qs = qs; o->w = w; o->pk = pk; o->pks = pks; o->fp8 = fp8;
+    o->H = H; o->D = D; o->P = P;
+    o->pkd = (double *)malloc(sizeof(double) * (size_t)(P > 0 ? P : 1) * D);
+    for (int64_t p = 0; p < P; p++)
+        for (int d = 0; d < D; d++) o->pkd[p * D + d] = pk_elem(o, p, d);
+}
+
+static void ops_free(ora_operands *o) { free(o->pkd); }
+
+/* qd: decoded q row of token t, [H, D] */
+static void decode_q(const ora_operands *o, int64_t t, double *qd)
+{
+    for (int h = 0; h < o->H; h++)
+        for (int d = 0; d < o->D; d++) qd[h * o->D + d] = q_elem(o, t, h, d);
+}
+
 /* score[t,p] = sum_h w[t,h] * relu( sum_d q[t,h,d] * pk[p,d] );
  * cond[t,p]  = sum_h |w[t,h]| * relu(...)   (the condition scale used by
  * the parity tolerance). */
-static void score_pair(const ora_operands *o, int64_t t, int64_t p, double *score, double *cond)
+static void score_pair(const ora_operands *o, const double *qd, int64_t t, int64_t p,
+                       double *score, double *cond)
 {
+    const double *kd = o->pkd + p * o->D;
     double sc = 0.0, cd = 0.0;
     for (int h = 0; h < o->H; h++) {
+        const double *qh = qd + h * o->D;
         double x = 0.0;
-        for (int d = 0; d < o->D; d++) x += q_elem(o, t, h, d) * pk_elem(o, p, d);
+        for (int d = 0; d < o->D; d++) x += qh[d] * kd[d];
         double r = x > 0.0 ? x : 0.0;
         double wv = (double)o->w[t * o->H + h];
         sc += wv * r;
@@ -359,26 +387,34 @@ static int64_t n_complete(int64_t tau, int kp) { return (tau + 1) / kp; }
  * is not a complete causal pool of the row's document gets -inf / 0. */
 void ora_score_pairs(const void *q, const float *qs, const float *w, const void *pk,
                      const float *pks, int fp8, const int32_t *cu_seqlens, int n_docs,
-                     int H, int D, int kp, const int64_t *rows, const int64_t *pools,
+                     int H, int D, int kp, int64_t P, const int64_t *rows, const int64_t *pools,
                      int64_t n_pairs, double *score_out, double *cond_out)
 {
-    ora_operands o = {q, qs, w, pk, pks, fp8, H, D};
+    ora_operands o;
+    ops_init(&o, q, qs, w, pk, pks, fp8, H, D, P);
     int32_t *cu_pools = (int32_t *)malloc(sizeof(int32_t) * (n_docs + 1));
     ora_cu_pools(cu_seqlens, n_docs, kp, cu_pools);
-#pragma omp parallel for schedule(dynamic, 16)
-    for (int64_t i = 0; i < n_pairs; i++) {
-        int64_t t = rows[i], p = pools[i];
-        int doc = doc_of_token(cu_seqlens, n_docs, t);
-        int64_t tau = t - cu_seqlens[doc];
-        int64_t j = p - cu_pools[doc];
-        if (doc < 0 || j < 0 || j >= n_complete(tau, kp)) {
-            score_out[i] = -INFINITY;
-            cond_out[i] = 0.0;
-            continue;
+#pragma omp parallel
+    {
+        double *qd = (double *)malloc(sizeof(double) * H * D);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < n_pairs; i++) {
+            int64_t t = rows[i], p = pools[i];
+            int doc = doc_of_token(cu_seqlens, n_docs, t);
+            int64_t tau = t - cu_seqlens[doc];
+            int64_t j = p - cu_pools[doc];
+            if (doc < 0 || j < 0 || j >= n_complete(tau, kp)) {
+                score_out[i] = -INFINITY;
+                cond_out[i] = 0.0;
+                continue;
+            }
+            decode_q(&o, t, qd);
+            score_pair(&o, qd, t, p, &score_out[i], &cond_out[i]);
         }
-        score_pair(&o, t, p, &score_out[i], &cond_out[i]);
+        free(qd);
     }
     free(cu_pools);
+    ops_free(&o);
 }
 
 typedef struct {
@@ -410,55 +446,64 @@ static int i64_cmp(const void *a, const void *b)
  *   n_sel[r]          number of selected pools. */
 void ora_select_rows(const void *q, const float *qs, const float *w, const void *pk,
                      const float *pks, int fp8, const int32_t *cu_seqlens, int n_docs,
-                     int H, int D, int kp, int Kp, const int64_t *rows, int64_t n_rows,
+                     int H, int D, int kp, int64_t P, int Kp, const int64_t *rows, int64_t n_rows,
                      int32_t *sel, double *sel_score, double *kth, double *kth_cond,
                      int32_t *n_sel)
 {
-    ora_operands o = {q, qs, w, pk, pks, fp8, H, D};
+    ora_operands o;
+    ops_init(&o, q, qs, w, pk, pks, fp8, H, D, P);
     int32_t *cu_pools = (int32_t *)malloc(sizeof(int32_t) * (n_docs + 1));
     ora_cu_pools(cu_seqlens, n_docs, kp, cu_pools);
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t r = 0; r < n_rows; r++) {
-        int64_t t = rows[r];
-        int doc = doc_of_token(cu_seqlens, n_docs, t);
-        int64_t tau = t - cu_seqlens[doc];
-        int64_t nc = n_complete(tau, kp);
-        cand *c = (cand *)malloc(sizeof(cand) * (nc > 0 ? nc : 1));
-        double *conds = (double *)malloc(sizeof(double) * (nc > 0 ? nc : 1));
-        for (int64_t j = 0; j < nc; j++) {
-            c[j].p = cu_pools[doc] + j;
-            score_pair(&o, t, c[j].p, &c[j].s, &conds[j]);
-        }
-        qsort(c, (size_t)nc, sizeof(cand), cand_cmp);
-        int64_t ns = nc < Kp ? nc : Kp;
-        n_sel[r] = (int32_t)ns;
-        if (nc > Kp) {
-            kth[r] = c[Kp - 1].s;
-            kth_cond[r] = conds[c[Kp - 1].p - cu_pools[doc]];
-        } else {
-            kth[r] = NAN;
-            kth_cond[r] = 0.0;
-        }
-        /* ascending pool order for output */
-        int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (ns > 0 ? ns : 1));
-        for (int64_t i = 0; i < ns; i++) idx[i] = c[i].p;
-        qsort(idx, (size_t)ns, sizeof(int64_t), i64_cmp);
-        for (int64_t i = 0; i < Kp; i++) {
-            if (i < ns) {
-                sel[r * Kp + i] = (int32_t)idx[i];
-                double s = 0, cd = 0;
-                score_pair(&o, t, idx[i], &s, &cd);
-                sel_score[r * Kp + i] = s;
-            } else {
-                sel[r * Kp + i] = -1;
-                sel_score[r * Kp + i] = -INFINITY;
+#pragma omp parallel
+    {
+        double *qd = (double *)malloc(sizeof(double) * H * D);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; r++) {
+            int64_t t = rows[r];
+            int doc = doc_of_token(cu_seqlens, n_docs, t);
+            int64_t tau = t - cu_seqlens[doc];
+            int64_t nc = n_complete(tau, kp);
+            cand *c = (cand *)malloc(sizeof(cand) * (nc > 0 ? nc : 1));
+            double *conds = (double *)malloc(sizeof(double) * (nc > 0 ? nc : 1));
+            double *scores = (double *)malloc(sizeof(double) * (nc > 0 ? nc : 1));
+            decode_q(&o, t, qd);
+            for (int64_t j = 0; j < nc; j++) {
+                c[j].p = cu_pools[doc] + j;
+                score_pair(&o, qd, t, c[j].p, &scores[j], &conds[j]);
+                c[j].s = scores[j];
             }
+            qsort(c, (size_t)nc, sizeof(cand), cand_cmp);
+            int64_t ns = nc < Kp ? nc : Kp;
+            n_sel[r] = (int32_t)ns;
+            if (nc > Kp) {
+                kth[r] = c[Kp - 1].s;
+                kth_cond[r] = conds[c[Kp - 1].p - cu_pools[doc]];
+            } else {
+                kth[r] = NAN;
+                kth_cond[r] = 0.0;
+            }
+            /* ascending pool order for output */
+            int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (ns > 0 ? ns : 1));
+            for (int64_t i = 0; i < ns; i++) idx[i] = c[i].p;
+            qsort(idx, (size_t)ns, sizeof(int64_t), i64_cmp);
+            for (int64_t i = 0; i < Kp; i++) {
+                if (i < ns) {
+                    sel[r * Kp + i] = (int32_t)idx[i];
+                    sel_score[r * Kp + i] = scores[idx[i] - cu_pools[doc]];
+                } else {
+                    sel[r * Kp + i] = -1;
+                    sel_score[r * Kp + i] = -INFINITY;
+                }
+            }
+            free(idx);
+            free(scores);
+            free(conds);
+            free(c);
         }
-        free(idx);
-        free(conds);
-        free(c);
+        free(qd);
     }
     free(cu_pools);
+    ops_free(&o);
 }
 
 /* Full score rows (small cases): out[r, p] for every global pool p, -inf
@@ -468,26 +513,34 @@ void ora_score_rows_full(const void *q, const float *qs, const float *w, const v
                          int H, int D, int kp, int64_t P_total, const int64_t *rows,
                          int64_t n_rows, double *out, double *cond_out)
 {
-    ora_operands o = {q, qs, w, pk, pks, fp8, H, D};
+    ora_operands o;
+    ops_init(&o, q, qs, w, pk, pks, fp8, H, D, P_total);
     int32_t *cu_pools = (int32_t *)malloc(sizeof(int32_t) * (n_docs + 1));
     ora_cu_pools(cu_seqlens, n_docs, kp, cu_pools);
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t r = 0; r < n_rows; r++) {
-        int64_t t = rows[r];
-        int doc = doc_of_token(cu_seqlens, n_docs, t);
-        int64_t tau = t - cu_seqlens[doc];
-        int64_t nc = n_complete(tau, kp);
-        for (int64_t p = 0; p < P_total; p++) {
-            int64_t j = p - cu_pools[doc];
-            if (j >= 0 && j < nc) {
-                score_pair(&o, t, p, &out[r * P_total + p], &cond_out[r * P_total + p]);
-            } else {
-                out[r * P_total + p] = -INFINITY;
-                cond_out[r * P_total + p] = 0.0;
+#pragma omp parallel
+    {
+        double *qd = (double *)malloc(sizeof(double) * H * D);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; r++) {
+            int64_t t = rows[r];
+            int doc = doc_of_token(cu_seqlens, n_docs, t);
+            int64_t tau = t - cu_seqlens[doc];
+            int64_t nc = n_complete(tau, kp);
+            decode_q(&o, t, qd);
+            for (int64_t p = 0; p < P_total; p++) {
+                int64_t j = p - cu_pools[doc];
+                if (j >= 0 && j < nc) {
+                    score_pair(&o, qd, t, p, &out[r * P_total + p], &cond_out[r * P_total + p]);
+                } else {
+                    out[r * P_total + p] = -INFINITY;
+                    cond_out[r * P_total + p] = 0.0;
+                }
             }
         }
+        free(qd);
     }
     free(cu_pools);
+    ops_free(&o);
 }
 
 /* ------------------------------------------------------------------ */

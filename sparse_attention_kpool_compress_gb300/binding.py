@@ -1,0 +1,273 @@
+"""Python binding of libkpool.so (the GB300-native KPool DSA indexer).
+
+Thin ctypes marshalling over the C ABI declared in ``include/kpool.h``: each
+function checks dtypes/devices, allocates outputs with torch (device memory
+and streams are torch's job here), and calls the C entry point of the same
+name on the current CUDA stream.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback of any kind -- importing this
+module fails loudly if ``libkpool.so`` has not been built.
+
+Sources (page titles and sections): Megatron-LM PR "GLM5.3 Flash (KDA + mHC +
+KPool DSA) support + FP8", Changes section 3 "KPool DSA indexer + NoPE";
+SkyRL PR "GLM-5.3-Flash (glm5_next) Megatron support", commit "k-pool
+indexer"; xtuner PR "GLM-5.3-Flash F5: NoPE DSA + KPool indexer".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkpool.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libkpool.so is not built (expected at %s); run "
+        "`python -c \"import __graft_entry__ as g; g.build()\"` or "
+        "`python sparse_attention_kpool_compress_gb300/build.py`" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "kpool_last_error": (ctypes.c_char_p, []),
+    "kpool_version": (_I, []),
+    "kpool_num_pools": (_I, [_P, _I, _L, _I, _P, _P]),
+    "kpool_cu_pools": (_I, [_P, _I, _I, _P, _P]),
+    "kpool_compress": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _L, _P, _P, _P, _P]),
+    "kpool_quantize_fp8": (_I, [_P, _L, _I, _P, _P, _P]),
+    "kpool_score_topk_workspace_size": (_SZ, [_L, _I, _I]),
+    "kpool_score_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I, _I,
+                              _P, _P, _P, _SZ, _P]),
+    "kpool_score_dense": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I,
+                               _P, _P, _SZ, _P]),
+    "kpool_expand_indices": (_I, [_P, _P, _P, _I, _L, _I, _I, _I, _P, _P]),
+    "kpool_read_status": (_I, [_P, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+STATUS_TIMEOUT = 1
+STATUS_BAD_SEQLENS = 2
+
+
+class KPoolError(RuntimeError):
+    def __init__(self, code, fn):
+        msg = _lib.kpool_last_error().decode(errors="replace")
+        super().__init__("%s failed (%d): %s" % (fn, code, msg))
+        self.code = code
+
+
+def _check(rc, fn):
+    if rc != 0:
+        raise KPoolError(rc, fn)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype=None, device=True):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if device and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def _as_u8(t):
+    if t is None:
+        return None
+    return t.view(torch.uint8) if t.dtype != torch.uint8 else t
+
+
+def _docs(cu_seqlens, cu_pools):
+    if cu_seqlens is None:
+        if cu_pools is not None:
+            raise ValueError("cu_pools given without cu_seqlens")
+        return 1
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    _need(cu_pools, "cu_pools", torch.int32)
+    return cu_seqlens.numel() - 1
+
+
+# ---------------------------------------------------------------------------
+
+def kpool_version() -> int:
+    return int(_lib.kpool_version())
+
+
+def kpool_num_pools(cu_seqlens_host, T: int, kpool: int):
+    """Host helper: (cu_pools int32 CPU tensor, total pools) from a host
+    cu_seqlens (list or CPU int32 tensor).  Validates the layout."""
+    cs = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous().cpu()
+    out = torch.empty_like(cs)
+    total = ctypes.c_int64(0)
+    _check(_lib.kpool_num_pools(_ptr(cs), cs.numel() - 1, T, kpool, _ptr(out),
+                                ctypes.byref(total)), "kpool_num_pools")
+    return out, int(total.value)
+
+
+def kpool_cu_pools(cu_seqlens: torch.Tensor, kpool: int) -> torch.Tensor:
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    out = torch.empty_like(cu_seqlens)
+    _check(_lib.kpool_cu_pools(_ptr(cu_seqlens), cu_seqlens.numel() - 1, kpool, _ptr(out),
+                               _stream(cu_seqlens.device)), "kpool_cu_pools")
+    return out
+
+
+def kpool_compress(k, gate, ape, kpool: int, cu_seqlens=None, cu_pools=None, P_total=None,
+                   fp8: bool = False, out=None):
+    """Pooled keys pk [P_total, D] bf16 (plus E4M3 codes and scales when
+    fp8).  For packed documents pass device cu_seqlens/cu_pools and P_total."""
+    _need(k, "k", torch.bfloat16)
+    _need(gate, "gate", torch.bfloat16)
+    _need(ape, "ape", torch.float32)
+    n_docs = _docs(cu_seqlens, cu_pools)
+    T, D = k.shape
+    if P_total is None:
+        if cu_seqlens is not None:
+            raise ValueError("P_total is required with cu_seqlens")
+        P_total = T // kpool
+    pk = out if out is not None else torch.empty(P_total, D, dtype=torch.bfloat16,
+                                                 device=k.device)
+    pk8 = sc = None
+    if fp8:
+        pk8 = torch.empty(P_total, D, dtype=torch.uint8, device=k.device)
+        sc = torch.empty(P_total, dtype=torch.float32, device=k.device)
+    _check(_lib.kpool_compress(_ptr(k), _ptr(gate), _ptr(ape), _ptr(cu_seqlens), _ptr(cu_pools),
+                               n_docs, T, D, kpool, P_total, _ptr(pk), _ptr(pk8), _ptr(sc),
+                               _stream(k.device)), "kpool_compress")
+    return (pk, pk8, sc) if fp8 else pk
+
+
+def kpool_quantize_fp8(x):
+    """x bf16 [..., 128] -> (E4M3 codes uint8 [..., 128], fp32 scales [...])."""
+    _need(x, "x", torch.bfloat16)
+    D = x.shape[-1]
+    rows = x.numel() // D
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _check(_lib.kpool_quantize_fp8(_ptr(x), rows, D, _ptr(codes), _ptr(sc), _stream(x.device)),
+           "kpool_quantize_fp8")
+    return codes, sc
+
+
+def kpool_score_topk_workspace_size(T: int, H: int, n_docs: int = 1) -> int:
+    return int(_lib.kpool_score_topk_workspace_size(T, H, n_docs))
+
+
+def new_workspace(T: int, H: int, n_docs: int = 1, device="cuda") -> torch.Tensor:
+    n = kpool_score_topk_workspace_size(T, H, n_docs)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def _score_common(q, w, pk, q_scale, pk_scale, cu_seqlens, cu_pools):
+    fp8 = q_scale is not None
+    if fp8:
+        _need(q, "q", (torch.uint8, torch.float8_e4m3fn))
+        _need(pk, "pk", (torch.uint8, torch.float8_e4m3fn))
+        _need(q_scale, "q_scale", torch.float32)
+        _need(pk_scale, "pk_scale", torch.float32)
+    else:
+        _need(q, "q", torch.bfloat16)
+        _need(pk, "pk", torch.bfloat16)
+    _need(w, "w", torch.float32)
+    n_docs = _docs(cu_seqlens, cu_pools)
+    T, H, D = q.shape
+    return fp8, n_docs, T, H, D, pk.shape[0]
+
+
+def kpool_score_topk(q, w, pk, kpool: int, index_topk: int, cu_seqlens=None, cu_pools=None,
+                     q_scale=None, pk_scale=None, workspace=None, out=None):
+    """(pool_idx int32 [T, Kp], pool_score fp32 [T, Kp]) -- ascending pools,
+    -1 / -inf padded."""
+    fp8, n_docs, T, H, D, P = _score_common(q, w, pk, q_scale, pk_scale, cu_seqlens, cu_pools)
+    Kp = index_topk // kpool
+    if workspace is None:
+        workspace = new_workspace(T, H, n_docs, q.device)
+    if out is None:
+        idx = torch.empty(T, Kp, dtype=torch.int32, device=q.device)
+        sc = torch.empty(T, Kp, dtype=torch.float32, device=q.device)
+    else:
+        idx, sc = out
+    _check(_lib.kpool_score_topk(_ptr(_as_u8(q)) if fp8 else _ptr(q), _ptr(q_scale), _ptr(w),
+                                 _ptr(_as_u8(pk)) if fp8 else _ptr(pk), _ptr(pk_scale),
+                                 _ptr(cu_seqlens), _ptr(cu_pools), n_docs, T, P, H, D, kpool,
+                                 index_topk, int(fp8), _ptr(idx), _ptr(sc), _ptr(workspace),
+                                 workspace.numel(), _stream(q.device)), "kpool_score_topk")
+    return idx, sc
+
+
+def kpool_score_dense(q, w, pk, kpool: int, cu_seqlens=None, cu_pools=None, q_scale=None,
+                      pk_scale=None, workspace=None):
+    """Test/debug: full fp32 [T, P] scores (-inf where not a causal pool)."""
+    fp8, n_docs, T, H, D, P = _score_common(q, w, pk, q_scale, pk_scale, cu_seqlens, cu_pools)
+    if workspace is None:
+        workspace = new_workspace(T, H, n_docs, q.device)
+    out = torch.empty(T, P, dtype=torch.float32, device=q.device)
+    _check(_lib.kpool_score_dense(_ptr(_as_u8(q)) if fp8 else _ptr(q), _ptr(q_scale), _ptr(w),
+                                  _ptr(_as_u8(pk)) if fp8 else _ptr(pk), _ptr(pk_scale),
+                                  _ptr(cu_seqlens), _ptr(cu_pools), n_docs, T, P, H, D, kpool,
+                                  int(fp8), _ptr(out), _ptr(workspace), workspace.numel(),
+                                  _stream(q.device)), "kpool_score_dense")
+    return out
+
+
+def kpool_expand_indices(pool_idx, kpool: int, index_topk: int, always_select_tail: bool = True,
+                         cu_seqlens=None, cu_pools=None, out=None):
+    """Token indices int32 [T, Kp*kpool + kpool - 1], ascending, -1 padded."""
+    _need(pool_idx, "pool_idx", torch.int32)
+    n_docs = _docs(cu_seqlens, cu_pools)
+    T = pool_idx.shape[0]
+    Kp = index_topk // kpool
+    W = Kp * kpool + kpool - 1
+    tok = out if out is not None else torch.empty(T, W, dtype=torch.int32, device=pool_idx.device)
+    _check(_lib.kpool_expand_indices(_ptr(pool_idx), _ptr(cu_seqlens), _ptr(cu_pools), n_docs, T,
+                                     kpool, index_topk, int(bool(always_select_tail)), _ptr(tok),
+                                     _stream(pool_idx.device)), "kpool_expand_indices")
+    return tok
+
+
+def kpool_read_status(workspace) -> int:
+    v = ctypes.c_int(0)
+    _check(_lib.kpool_read_status(_ptr(workspace), ctypes.byref(v)), "kpool_read_status")
+    return int(v.value)
+
+
+def kpool_indexer_forward(q, k, gate, ape, w, kpool: int, index_topk: int,
+                          always_select_tail: bool = True, cu_seqlens=None, cu_pools=None,
+                          P_total=None, fp8: bool = False, workspace=None):
+    """The whole indexer path on the current stream: compress -> (FP8 cast of
+    q and pooled keys) -> score + top-k -> expand.  Returns
+    (tok_idx, pool_idx, pool_score)."""
+    if fp8:
+        pk, pk8, pks = kpool_compress(k, gate, ape, kpool, cu_seqlens, cu_pools, P_total, fp8=True)
+        q8, qs = kpool_quantize_fp8(q)
+        idx, sc = kpool_score_topk(q8, w, pk8, kpool, index_topk, cu_seqlens, cu_pools,
+                                   q_scale=qs, pk_scale=pks, workspace=workspace)
+    else:
+        pk = kpool_compress(k, gate, ape, kpool, cu_seqlens, cu_pools, P_total)
+        idx, sc = kpool_score_topk(q, w, pk, kpool, index_topk, cu_seqlens, cu_pools,
+                                   workspace=workspace)
+    tok = kpool_expand_indices(idx, kpool, index_topk, always_select_tail, cu_seqlens, cu_pools)
+    return tok, idx, sc
+
+
+__all__ = [n for n in dir() if n.startswith("kpool_")] + ["KPoolError", "new_workspace",
+                                                           "LIB_PATH"]

@@ -1,0 +1,311 @@
+// C ABI of libkpool.so: host-side argument checks, then one or two kernel
+// launches per call on the caller's stream.  See include/kpool.h for the
+// contract of every entry point.
+#include <cstdarg>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kpool_internal.h"
+
+namespace kpool {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+void set_error(const std::string &msg) { g_last_error = msg; }
+void clear_error() { g_last_error.clear(); }
+const char *last_error_cstr() { return g_last_error.c_str(); }
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    set_error(buf);
+    return code;
+}
+
+int num_sms()
+{
+    static std::mutex mu;
+    static std::vector<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lk(mu);
+    if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, 0);
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
+int check_docs(const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs, int64_t T,
+               int kpool, int64_t P_total)
+{
+    if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1 (got %d)", n_docs);
+    if ((cu_seqlens == nullptr) != (cu_pools == nullptr))
+        return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens and cu_pools must both be NULL or both set");
+    if (cu_seqlens == nullptr) {
+        if (n_docs != 1)
+            return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be 1 when cu_seqlens is NULL");
+        if (P_total >= 0 && P_total != T / kpool)
+            return fail(KPOOL_ERR_INVALID_ARG, "P_total must be T / kpool for one sequence");
+    } else {
+        if (!aligned(cu_seqlens, 4) || !aligned(cu_pools, 4))
+            return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens / cu_pools must be 4-byte aligned");
+    }
+    if (P_total > T) return fail(KPOOL_ERR_INVALID_ARG, "P_total exceeds T");
+    return KPOOL_OK;
+}
+
+}  // namespace kpool
+
+using namespace kpool;
+
+namespace {
+
+int check_common(int64_t T, int kpool)
+{
+    if (T < 0 || T > 0x7FFFFFFFLL) return fail(KPOOL_ERR_INVALID_ARG, "T out of range");
+    if (kpool < 1 || kpool > 64)
+        return fail(KPOOL_ERR_UNSUPPORTED, "kpool must be in [1, 64] (got %d)", kpool);
+    return KPOOL_OK;
+}
+
+int check_h(int H)
+{
+    if (H != 4 && H != 8 && H != 16 && H != 32 && H != 64 && H != 128)
+        return fail(KPOOL_ERR_UNSUPPORTED, "H must be one of 4, 8, 16, 32, 64, 128 (got %d)", H);
+    return KPOOL_OK;
+}
+
+int check_score_args(const void *q, const float *q_scale, const float *w, const void *pk,
+                     const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
+                     int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool, int fp8,
+                     void *workspace, size_t workspace_bytes)
+{
+    int rc = check_common(T, kpool);
+    if (rc) return rc;
+    if ((rc = check_h(H))) return rc;
+    if (fp8) {
+        if (D != 128) return fail(KPOOL_ERR_UNSUPPORTED, "FP8 mode needs D = 128 (got %d)", D);
+        if (!q_scale || !pk_scale)
+            return fail(KPOOL_ERR_INVALID_ARG, "FP8 mode needs q_scale and pk_scale");
+        if (!aligned(q_scale, 16) || !aligned(pk_scale, 4))
+            return fail(KPOOL_ERR_INVALID_ARG, "q_scale must be 16-byte aligned");
+    } else {
+        if (D != 32 && D != 64 && D != 128)
+            return fail(KPOOL_ERR_UNSUPPORTED, "D must be 32, 64 or 128 (got %d)", D);
+        if (q_scale || pk_scale)
+            return fail(KPOOL_ERR_INVALID_ARG, "q_scale / pk_scale must be NULL in bf16 mode");
+    }
+    if (T > 0 && (!q || !w)) return fail(KPOOL_ERR_INVALID_ARG, "q and w must be non-NULL");
+    if (P_total > 0 && !pk) return fail(KPOOL_ERR_INVALID_ARG, "pk must be non-NULL");
+    if (!aligned(q, 16) || !aligned(pk, 16) || !aligned(w, 16))
+        return fail(KPOOL_ERR_INVALID_ARG, "q, pk and w must be 16-byte aligned");
+    if (P_total < 0) return fail(KPOOL_ERR_INVALID_ARG, "P_total < 0");
+    if (static_cast<int64_t>(T) * H > 0x7FFFFFFFLL)
+        return fail(KPOOL_ERR_UNSUPPORTED, "T * H exceeds 2^31 - 1");
+    if ((rc = check_docs(cu_seqlens, cu_pools, n_docs, T, kpool, P_total))) return rc;
+    const size_t need = score_workspace_bytes(T, H, n_docs);
+    if (!workspace || workspace_bytes < need)
+        return fail(KPOOL_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need,
+                    workspace ? workspace_bytes : static_cast<size_t>(0));
+    if (!aligned(workspace, 256))
+        return fail(KPOOL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    return KPOOL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kpool_last_error(void) { return last_error_cstr(); }
+
+int kpool_version(void) { return 10000; }
+
+int kpool_num_pools(const int32_t *cu_seqlens_host, int n_docs, int64_t T, int kpool,
+                    int32_t *cu_pools_host_out, int64_t *total_pools_out)
+{
+    clear_error();
+    int rc = check_common(T, kpool);
+    if (rc) return rc;
+    if (!cu_seqlens_host || !cu_pools_host_out || !total_pools_out)
+        return fail(KPOOL_ERR_INVALID_ARG, "NULL pointer");
+    if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1");
+    if (cu_seqlens_host[0] != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens[0] must be 0 (got %d)", cu_seqlens_host[0]);
+    if (cu_seqlens_host[n_docs] != T)
+        return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens[n_docs] must equal T");
+    int64_t acc = 0;
+    cu_pools_host_out[0] = 0;
+    for (int d = 0; d < n_docs; ++d) {
+        const int64_t L = static_cast<int64_t>(cu_seqlens_host[d + 1]) - cu_seqlens_host[d];
+        if (L < 0) return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens decreases at document %d", d);
+        acc += L / kpool;
+        cu_pools_host_out[d + 1] = static_cast<int32_t>(acc);
+    }
+    *total_pools_out = acc;
+    return KPOOL_OK;
+}
+
+int kpool_cu_pools(const int32_t *cu_seqlens, int n_docs, int kpool, int32_t *cu_pools_out,
+                   kpool_stream_t stream)
+{
+    clear_error();
+    if (kpool < 1 || kpool > 64) return fail(KPOOL_ERR_UNSUPPORTED, "kpool must be in [1, 64]");
+    if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1");
+    if (!cu_seqlens || !cu_pools_out) return fail(KPOOL_ERR_INVALID_ARG, "NULL pointer");
+    KPOOL_CUDA_CHECK(launch_cu_pools(cu_seqlens, n_docs, kpool, cu_pools_out,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+    return KPOOL_OK;
+}
+
+int kpool_compress(const void *k, const void *gate, const float *ape,
+                   const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs,
+                   int64_t T, int D, int kpool, int64_t P_total, void *pk_out,
+                   uint8_t *pk_fp8_out, float *pk_scale_out, kpool_stream_t stream)
+{
+    clear_error();
+    int rc = check_common(T, kpool);
+    if (rc) return rc;
+    if (D != 32 && D != 64 && D != 128)
+        return fail(KPOOL_ERR_UNSUPPORTED, "D must be 32, 64 or 128 (got %d)", D);
+    if (P_total < 0) return fail(KPOOL_ERR_INVALID_ARG, "P_total < 0");
+    if ((rc = check_docs(cu_seqlens, cu_pools, n_docs, T, kpool, P_total))) return rc;
+    if (P_total > 0 && (!k || !gate || !ape || !pk_out))
+        return fail(KPOOL_ERR_INVALID_ARG, "k, gate, ape and pk_out must be non-NULL");
+    if (!aligned(k, 16) || !aligned(gate, 16) || !aligned(pk_out, 16) || !aligned(ape, 16))
+        return fail(KPOOL_ERR_INVALID_ARG, "k, gate, ape and pk_out must be 16-byte aligned");
+    if ((pk_fp8_out == nullptr) != (pk_scale_out == nullptr))
+        return fail(KPOOL_ERR_INVALID_ARG, "pk_fp8_out and pk_scale_out go together");
+    if (pk_fp8_out) {
+        if (D != 128) return fail(KPOOL_ERR_UNSUPPORTED, "FP8 pooled keys need D = 128");
+        if (!aligned(pk_fp8_out, 16) || !aligned(pk_scale_out, 4))
+            return fail(KPOOL_ERR_INVALID_ARG, "pk_fp8_out must be 16-byte aligned");
+    }
+    KPOOL_CUDA_CHECK(launch_compress(k, gate, ape, cu_seqlens, cu_pools, n_docs, T, D, kpool,
+                                     P_total, pk_out, pk_fp8_out, pk_scale_out,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+    return KPOOL_OK;
+}
+
+int kpool_quantize_fp8(const void *x, int64_t rows, int D, uint8_t *x_fp8_out, float *scale_out,
+                       kpool_stream_t stream)
+{
+    clear_error();
+    if (D != 128) return fail(KPOOL_ERR_UNSUPPORTED, "FP8 rows need D = 128 (got %d)", D);
+    if (rows < 0) return fail(KPOOL_ERR_INVALID_ARG, "rows < 0");
+    if (rows > 0 && (!x || !x_fp8_out || !scale_out))
+        return fail(KPOOL_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(x, 16) || !aligned(x_fp8_out, 16) || !aligned(scale_out, 4))
+        return fail(KPOOL_ERR_INVALID_ARG, "x and x_fp8_out must be 16-byte aligned");
+    KPOOL_CUDA_CHECK(launch_quantize_fp8(x, rows, x_fp8_out, scale_out,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    return KPOOL_OK;
+}
+
+size_t kpool_score_topk_workspace_size(int64_t T, int H, int n_docs)
+{
+    if (T < 0 || n_docs < 1 || check_h(H) != KPOOL_OK) return 0;
+    return score_workspace_bytes(T, H, n_docs);
+}
+
+int kpool_score_topk(const void *q, const float *q_scale, const float *w, const void *pk,
+                     const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
+                     int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool,
+                     int index_topk, int fp8, int32_t *pool_idx_out, float *pool_score_out,
+                     void *workspace, size_t workspace_bytes, kpool_stream_t stream)
+{
+    clear_error();
+    int rc = check_score_args(q, q_scale, w, pk, pk_scale, cu_seqlens, cu_pools, n_docs, T,
+                              P_total, H, D, kpool, fp8, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (index_topk < 1 || index_topk % kpool != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
+    const int Kp = index_topk / kpool;
+    const int cap = score_capacity(H, D, fp8);
+    if (Kp + 128 > cap)
+        return fail(KPOOL_ERR_UNSUPPORTED,
+                    "index_topk / kpool = %d exceeds the per-query capacity %d - 128 for H=%d",
+                    Kp, cap, H);
+    if (T > 0 && (!pool_idx_out || !pool_score_out))
+        return fail(KPOOL_ERR_INVALID_ARG, "pool_idx_out and pool_score_out must be non-NULL");
+    ScoreArgs a{};
+    a.q = q; a.q_scale = q_scale; a.w = w; a.pk = pk; a.pk_scale = pk_scale;
+    a.cu_seqlens = cu_seqlens; a.cu_pools = cu_pools; a.n_docs = n_docs;
+    a.T = T; a.P_total = P_total; a.H = H; a.D = D; a.kpool = kpool; a.Kp = Kp;
+    a.fp8 = fp8 ? 1 : 0; a.mode = 0;
+    a.pool_idx = pool_idx_out; a.pool_score = pool_score_out; a.scores = nullptr;
+    a.ws = static_cast<int *>(workspace); a.ws_bytes = workspace_bytes;
+    return run_score(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kpool_score_dense(const void *q, const float *q_scale, const float *w, const void *pk,
+                      const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
+                      int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool, int fp8,
+                      float *scores_out, void *workspace, size_t workspace_bytes,
+                      kpool_stream_t stream)
+{
+    clear_error();
+    int rc = check_score_args(q, q_scale, w, pk, pk_scale, cu_seqlens, cu_pools, n_docs, T,
+                              P_total, H, D, kpool, fp8, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (T > 0 && P_total > 0 && !scores_out)
+        return fail(KPOOL_ERR_INVALID_ARG, "scores_out must be non-NULL");
+    if (static_cast<double>(T) * static_cast<double>(P_total) > 4.0e9)
+        return fail(KPOOL_ERR_UNSUPPORTED, "dense scores are meant for small T");
+    ScoreArgs a{};
+    a.q = q; a.q_scale = q_scale; a.w = w; a.pk = pk; a.pk_scale = pk_scale;
+    a.cu_seqlens = cu_seqlens; a.cu_pools = cu_pools; a.n_docs = n_docs;
+    a.T = T; a.P_total = P_total; a.H = H; a.D = D; a.kpool = kpool; a.Kp = 1;
+    a.fp8 = fp8 ? 1 : 0; a.mode = 1;
+    a.pool_idx = nullptr; a.pool_score = nullptr; a.scores = scores_out;
+    a.ws = static_cast<int *>(workspace); a.ws_bytes = workspace_bytes;
+    return run_score(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kpool_expand_indices(const int32_t *pool_idx, const int32_t *cu_seqlens,
+                         const int32_t *cu_pools, int n_docs, int64_t T, int kpool,
+                         int index_topk, int always_select_tail, int32_t *tok_idx_out,
+                         kpool_stream_t stream)
+{
+    clear_error();
+    int rc = check_common(T, kpool);
+    if (rc) return rc;
+    if (index_topk < 1 || index_topk % kpool != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
+    if ((rc = check_docs(cu_seqlens, cu_pools, n_docs, T, kpool, -1))) return rc;
+    if (T > 0 && (!pool_idx || !tok_idx_out))
+        return fail(KPOOL_ERR_INVALID_ARG, "pool_idx and tok_idx_out must be non-NULL");
+    if (!aligned(pool_idx, 4) || !aligned(tok_idx_out, 4))
+        return fail(KPOOL_ERR_INVALID_ARG, "pool_idx and tok_idx_out must be 4-byte aligned");
+    const int Kp = index_topk / kpool;
+    if (static_cast<int64_t>(Kp) * kpool + kpool > 0x7FFFFFFF)
+        return fail(KPOOL_ERR_UNSUPPORTED, "row width overflows");
+    KPOOL_CUDA_CHECK(launch_expand(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp,
+                                   always_select_tail ? 1 : 0, tok_idx_out,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+    return KPOOL_OK;
+}
+
+int kpool_read_status(const void *workspace, int *status_out)
+{
+    clear_error();
+    if (!workspace || !status_out) return fail(KPOOL_ERR_INVALID_ARG, "NULL pointer");
+    KPOOL_CUDA_CHECK(cudaDeviceSynchronize());
+    int v = 0;
+    KPOOL_CUDA_CHECK(cudaMemcpy(&v, static_cast<const int *>(workspace) + 1, sizeof(int),
+                                cudaMemcpyDeviceToHost));
+    *status_out = v;
+    return KPOOL_OK;
+}
+
+}  // extern "C"

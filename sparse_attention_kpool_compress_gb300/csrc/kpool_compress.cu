@@ -1,0 +1,250 @@
+// Pool compression and the FP8 indexer-input emulation.
+//
+// Compression (Megatron-LM PR "GLM5.3 Flash (KDA + mHC + KPool DSA) support +
+// FP8", Changes section 3; SkyRL PR "GLM-5.3-Flash (glm5_next) Megatron
+// support", commit "k-pool indexer"): every dimension of a pool takes a
+// softmax over the pool's kpool slots of gate + ape, the weighted keys are
+// summed in FP32 and rounded once to BF16.
+//
+// FP8 emulation (same Megatron-LM section): FP32 Hadamard rotation -> BF16 ->
+// E4M3 with a power-of-two scale per 128-element row.
+//
+// Both are HBM streams.  One thread owns 8 consecutive dimensions (one 16-byte
+// vector) of one pool or row; a 128-dim row is 16 lanes of one warp, so the
+// 128-point Walsh-Hadamard transform runs as 3 in-thread butterfly stages and
+// 4 xor-shuffle stages.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "kpool_internal.h"
+
+namespace kpool {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float x)
+{
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return static_cast<uint32_t>(*reinterpret_cast<uint16_t *>(&b));
+}
+
+// Last document whose pool range starts at or before pool g (skips empty
+// documents that share the same start).
+__device__ __forceinline__ int find_doc(const int32_t *cu, int n_docs, int64_t g)
+{
+    int lo = 0, hi = n_docs;   // answer in [0, n_docs)
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (cu[mid] <= g) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// FP8 emulation of one 128-element row held by a 16-lane group (8 values per
+// lane, lane v owns elements 8v..8v+7).  Writes this lane's 8 E4M3 codes and,
+// from lane v == 0, the row scale.
+__device__ __forceinline__ void fp8_row(float (&x)[8], int v, uint8_t *codes8, float *scale_out,
+                                        bool active)
+{
+    // Walsh-Hadamard butterflies in natural (Sylvester) order, FP32.
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if ((i & h) == 0) {
+                float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float o = __shfl_xor_sync(0xFFFFFFFFu, x[i], m);
+            x[i] = (v & m) ? (o - x[i]) : (x[i] + o);
+        }
+    }
+    const float norm = 0.08838834764831845f;   // 128^-1/2
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[i] = __uint_as_float(bf16_bits_rn(x[i] * norm) << 16);
+        amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    // smallest power of two s with amax <= 448 s: amax = f * 2^E, f in [0.5, 1),
+    // 448 = 0.875 * 2^9  ->  s = 2^(E - 9 + (f > 0.875)).
+    float s = 1.f;
+    if (amax > 0.f) {
+        int E;
+        float f = frexpf(amax, &E);
+        s = ldexpf(1.f, E - 9 + (f > 0.875f ? 1 : 0));
+    }
+    if (!active) return;
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t c = static_cast<uint32_t>(
+            __nv_cvt_float_to_fp8(__fdiv_rn(x[i], s), __NV_SATFINITE, __NV_E4M3));
+        if (i < 4) lo |= c << (8 * i);
+        else hi |= c << (8 * (i - 4));
+    }
+    *reinterpret_cast<uint2 *>(codes8) = make_uint2(lo, hi);
+    if (v == 0) *scale_out = s;
+}
+
+__global__ void __launch_bounds__(kThreads) compress_kernel(
+    const uint16_t *__restrict__ k, const uint16_t *__restrict__ gate,
+    const float *__restrict__ ape, const int32_t *__restrict__ cu_seqlens,
+    const int32_t *__restrict__ cu_pools, int n_docs, int D, int kp, int64_t P_total,
+    uint16_t *__restrict__ pk, uint8_t *__restrict__ pk_fp8, float *__restrict__ pk_scale)
+{
+    const int vpr = D >> 3;
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t g = gid / vpr;
+    const int v = static_cast<int>(gid - g * vpr);
+    const bool active = g < P_total;
+
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+
+    if (active) {
+        int64_t tok0;
+        if (cu_pools != nullptr) {
+            int d = find_doc(cu_pools, n_docs, g);
+            tok0 = static_cast<int64_t>(cu_seqlens[d]) + (g - cu_pools[d]) * kp;
+        } else {
+            tok0 = g * kp;
+        }
+        const int col = v * 8;
+        float m[8], z[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; z[i] = 0.f; }
+        // softmax over slots of a_s = gate + ape, per dimension
+        for (int s = 0; s < kp; ++s) {
+            float gv[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(gate + (tok0 + s) * D + col), gv);
+            const float4 a0 = *reinterpret_cast<const float4 *>(ape + s * D + col);
+            const float4 a1 = *reinterpret_cast<const float4 *>(ape + s * D + col + 4);
+            const float ap[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], gv[i] + ap[i]);
+        }
+        for (int s = 0; s < kp; ++s) {
+            float gv[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(gate + (tok0 + s) * D + col), gv);
+            const float4 a0 = *reinterpret_cast<const float4 *>(ape + s * D + col);
+            const float4 a1 = *reinterpret_cast<const float4 *>(ape + s * D + col + 4);
+            const float ap[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) z[i] += expf((gv[i] + ap[i]) - m[i]);
+        }
+        for (int s = 0; s < kp; ++s) {
+            float gv[8], kv[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(gate + (tok0 + s) * D + col), gv);
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(k + (tok0 + s) * D + col), kv);
+            const float4 a0 = *reinterpret_cast<const float4 *>(ape + s * D + col);
+            const float4 a1 = *reinterpret_cast<const float4 *>(ape + s * D + col + 4);
+            const float ap[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float alpha = __fdiv_rn(expf((gv[i] + ap[i]) - m[i]), z[i]);
+                acc[i] = fmaf(alpha, kv[i], acc[i]);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = bf16_bits_rn(acc[2 * i]) | (bf16_bits_rn(acc[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4 *>(pk + g * D + col) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+
+    if (pk_fp8 != nullptr) {   // D == 128: a row is 16 lanes of this warp
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(bf16_bits_rn(acc[i]) << 16);
+        fp8_row(x, v, pk_fp8 + (active ? g : 0) * 128 + v * 8, pk_scale + (active ? g : 0),
+                active);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) quantize_fp8_kernel(
+    const uint16_t *__restrict__ x, int64_t rows, uint8_t *__restrict__ out,
+    float *__restrict__ scale)
+{
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t r = gid >> 4;
+    const int v = static_cast<int>(gid & 15);
+    const bool active = r < rows;
+    float f[8];
+    if (active) {
+        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(x + r * 128 + v * 8), f);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    }
+    fp8_row(f, v, out + (active ? r : 0) * 128 + v * 8, scale + (active ? r : 0), active);
+}
+
+__global__ void cu_pools_kernel(const int32_t *cu_seqlens, int n_docs, int kp, int32_t *cu_pools)
+{
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    int32_t acc = 0;
+    cu_pools[0] = 0;
+    for (int d = 0; d < n_docs; ++d) {
+        acc += (cu_seqlens[d + 1] - cu_seqlens[d]) / kp;
+        cu_pools[d + 1] = acc;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_cu_pools(const int32_t *cu_seqlens, int n_docs, int kpool, int32_t *cu_pools,
+                            cudaStream_t s)
+{
+    cu_pools_kernel<<<1, 32, 0, s>>>(cu_seqlens, n_docs, kpool, cu_pools);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compress(const void *k, const void *gate, const float *ape,
+                            const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs,
+                            int64_t T, int D, int kpool, int64_t P_total, void *pk_out,
+                            uint8_t *pk_fp8, float *pk_scale, cudaStream_t s)
+{
+    (void)T;
+    if (P_total == 0) return cudaSuccess;
+    const int64_t threads = P_total * (D / 8);
+    const int64_t blocks = (threads + kThreads - 1) / kThreads;
+    compress_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+        static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(gate), ape, cu_seqlens,
+        cu_pools, n_docs, D, kpool, P_total, static_cast<uint16_t *>(pk_out), pk_fp8, pk_scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8(const void *x, int64_t rows, uint8_t *out, float *scale,
+                                cudaStream_t s)
+{
+    if (rows == 0) return cudaSuccess;
+    const int64_t blocks = (rows * 16 + kThreads - 1) / kThreads;
+    quantize_fp8_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+        static_cast<const uint16_t *>(x), rows, out, scale);
+    return cudaGetLastError();
+}
+
+}  // namespace kpool

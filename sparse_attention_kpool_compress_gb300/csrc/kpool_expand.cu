@@ -1,0 +1,86 @@
+// Expansion of selected pools to token indices plus the causal tail
+// (Megatron-LM PR "GLM5.3 Flash (KDA + mHC + KPool DSA) support + FP8",
+// Changes section 3: top-k pools are expanded back to token indices;
+// always_select_tail appends each query's incomplete causal pool; packed THD
+// restarts pools at document boundaries).
+//
+// HBM-write-bound: one warp per query row, lanes stride over the
+// Kp*kpool + kpool - 1 outputs of the row (128-byte coalesced stores).
+#include "kpool_internal.h"
+
+namespace kpool {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRowsPerBlock = kThreads / 32;
+
+__device__ __forceinline__ int doc_of_token(const int32_t *cu, int n_docs, int64_t t)
+{
+    int lo = 0, hi = n_docs;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (cu[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+template <int KP>   // KP > 0: compile-time kpool; 0: runtime kp
+__global__ void __launch_bounds__(kThreads) expand_kernel(
+    const int32_t *__restrict__ pool_idx, const int32_t *__restrict__ cu_seqlens,
+    const int32_t *__restrict__ cu_pools, int n_docs, int64_t T, int kp_rt, int Kp, int tail,
+    int32_t *__restrict__ out)
+{
+    const int kp = KP > 0 ? KP : kp_rt;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    int64_t doc_start = 0, pool_lo = 0, pool_hi = T / kp;
+    if (cu_seqlens != nullptr) {
+        const int d = doc_of_token(cu_seqlens, n_docs, t);
+        doc_start = cu_seqlens[d];
+        pool_lo = cu_pools[d];
+        pool_hi = cu_pools[d + 1];
+    }
+    const int64_t tau = t - doc_start;
+    const int64_t nc = (tau + 1) / kp;
+    const int n_sel = static_cast<int>(nc < Kp ? nc : Kp);
+    const int n_pool_tok = n_sel * kp;
+    const int n_tail = tail ? static_cast<int>((tau + 1) - nc * kp) : 0;
+    const int W = Kp * kp + kp - 1;
+    const int32_t *row_in = pool_idx + t * Kp;
+    int32_t *row_out = out + t * W;
+    for (int c = lane; c < W; c += 32) {
+        int32_t v = -1;
+        if (c < n_pool_tok) {
+            const int e = c / kp;
+            const int s = c - e * kp;
+            const int32_t g = row_in[e];
+            if (g >= pool_lo && g < pool_hi)
+                v = static_cast<int32_t>(doc_start + (g - pool_lo) * kp + s);
+        } else if (c < n_pool_tok + n_tail) {
+            v = static_cast<int32_t>(t - n_tail + 1 + (c - n_pool_tok));
+        }
+        row_out[c] = v;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_expand(const int32_t *pool_idx, const int32_t *cu_seqlens,
+                          const int32_t *cu_pools, int n_docs, int64_t T, int kpool, int Kp,
+                          int tail, int32_t *tok_idx, cudaStream_t s)
+{
+    if (T == 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>((T + kRowsPerBlock - 1) / kRowsPerBlock);
+    switch (kpool) {
+    case 1: expand_kernel<1><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    case 2: expand_kernel<2><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    case 4: expand_kernel<4><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    case 8: expand_kernel<8><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    default: expand_kernel<0><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kpool

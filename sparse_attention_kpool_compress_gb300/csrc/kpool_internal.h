@@ -1,0 +1,72 @@
+// Host-side helpers shared by the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "../../include/kpool.h"
+
+namespace kpool {
+
+// Thread-local message of the last failing call (kpool_last_error).
+void set_error(const std::string &msg);
+void clear_error();
+const char *last_error_cstr();
+
+int fail(int code, const char *fmt, ...);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define KPOOL_CUDA_CHECK(expr)                                                            \
+    do {                                                                                  \
+        cudaError_t e_ = (expr);                                                          \
+        if (e_ != cudaSuccess)                                                            \
+            return ::kpool::fail(KPOOL_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+    } while (0)
+
+// Validation of the document layout arguments shared by several entry points.
+int check_docs(const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs, int64_t T,
+               int kpool, int64_t P_total);
+
+// ---- launchers implemented in the .cu files ----------------------------
+cudaError_t launch_cu_pools(const int32_t *cu_seqlens, int n_docs, int kpool, int32_t *cu_pools,
+                            cudaStream_t s);
+cudaError_t launch_compress(const void *k, const void *gate, const float *ape,
+                            const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs,
+                            int64_t T, int D, int kpool, int64_t P_total, void *pk_out,
+                            uint8_t *pk_fp8, float *pk_scale, cudaStream_t s);
+cudaError_t launch_quantize_fp8(const void *x, int64_t rows, uint8_t *out, float *scale,
+                                cudaStream_t s);
+cudaError_t launch_expand(const int32_t *pool_idx, const int32_t *cu_seqlens,
+                          const int32_t *cu_pools, int n_docs, int64_t T, int kpool, int Kp,
+                          int tail, int32_t *tok_idx, cudaStream_t s);
+
+// Scoring (kpool_score.cu).  mode 0 = top-k, 1 = dense scores.
+struct ScoreArgs {
+    const void *q;
+    const float *q_scale;
+    const float *w;
+    const void *pk;
+    const float *pk_scale;
+    const int32_t *cu_seqlens;
+    const int32_t *cu_pools;
+    int n_docs;
+    int64_t T;
+    int64_t P_total;
+    int H, D, kpool, Kp, fp8, mode;
+    int32_t *pool_idx;
+    float *pool_score;
+    float *scores;
+    int *ws;              // workspace header + schedule table
+    size_t ws_bytes;
+};
+size_t score_workspace_bytes(int64_t T, int H, int n_docs);
+int score_capacity(int H, int D, int fp8);   // candidate slots per query (0 = unsupported)
+int run_score(const ScoreArgs &a, cudaStream_t s);
+
+}  // namespace kpool

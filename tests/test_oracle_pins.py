@@ -498,3 +498,14 @@ def test_packed_equals_per_document(ora):
         sel_d = np.where(od["sel"] >= 0, od["sel"] + cp[d], -1)
         assert np.array_equal(out["sel"][a:b], sel_d)
         assert np.array_equal(exp[a:b], np.where(ed >= 0, ed + a, -1))
+
+
+def test_compress_condition_scale(ora):
+    """cond = sum_s alpha_s |k_s| >= |pk_exact|, with equality when all keys
+    of a pool share a sign."""
+    kb, gb, ape = _rand_inputs(64, 32, 4, seed=8)
+    pk, ex, cond = ora.compress(kb, gb, ape, None, 4, want_cond=True)
+    assert np.all(cond >= np.abs(ex) * (1 - 1e-15))
+    kp_ = kb & 0x7FFF
+    _, ex2, cond2 = ora.compress(kp_, gb, ape, None, 4, want_cond=True)
+    assert np.allclose(cond2, ex2, rtol=1e-15, atol=0)
