@@ -220,13 +220,18 @@ def main():
     ap.add_argument("--workload", default="long_128k", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--baseline-rows", type=int, default=96)
+    ap.add_argument("--baseline-rows", type=int, default=1536)
     ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--T", type=int, default=None,
+                    help="same recipe at another token count (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warmup raised to 3 (minimum)", file=sys.stderr)
         args.warmup = 3
     wl = W.WORKLOADS[args.workload]
+    if args.T is not None:
+        from dataclasses import replace
+        wl = replace(wl, T=args.T, name="%s_T%d" % (wl.name, args.T))
     if args.impl == "reference":
         return run_reference(args, wl)
 
