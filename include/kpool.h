@@ -176,6 +176,38 @@ KPOOL_API int kpool_score_topk(const void *q, const float *q_scale, const float 
                      void *workspace, size_t workspace_bytes, kpool_stream_t stream);
 
 /*
+ * kpool_score_topk_noalloc -- the same computation, arguments and outputs as
+ * kpool_score_topk, for callers that cannot allocate device memory: code
+ * running where cudaMalloc is not allowed or not wanted, such as inside a
+ * framework's custom-op or plugin hook that only hands out its input and
+ * output buffers, or an inference runtime that reserves all device memory
+ * up front and forbids allocation afterwards.  (The pages have no
+ * counterpart of this entry point.)
+ *   - No workspace argument: the scratch (tile counter, status word and
+ *     query-tile schedule) lives in a fixed array inside the library, about
+ *     1 MiB, held on every device that loads the library until the process
+ *     exits.  This call itself allocates nothing.
+ *   - Capacity: ceil(T / (256 / H)) + n_docs <= 131072 query tiles (e.g.
+ *     T up to 524288 - 4 * n_docs tokens at H = 64).  Larger inputs are
+ *     rejected with KPOOL_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array.  Each call rewrites
+ *     everything it reads from it before use, but calls that overlap on the
+ *     GPU (different streams, or host threads) race on it and must be
+ *     serialised by the caller.
+ *   - The status word it writes is not exposed; validate cu_seqlens on the
+ *     host (kpool_num_pools) when its values are untrusted.
+ */
+KPOOL_API int kpool_score_topk_noalloc(const void *q, const float *q_scale, const float *w,
+                                       const void *pk, const float *pk_scale,
+                                       const int32_t *cu_seqlens, const int32_t *cu_pools,
+                                       int n_docs, int64_t T, int64_t P_total, int H, int D,
+                                       int kpool, int index_topk, int fp8, int32_t *pool_idx_out,
+                                       float *pool_score_out, kpool_stream_t stream);
+
+/*
  * kpool_score_dense -- test/debug entry: the same scoring as
  * kpool_score_topk (same kernel pipeline, no selection) written out in full:
  * scores_out[t, p] (fp32 [T, P_total]) for every complete causal pool p of

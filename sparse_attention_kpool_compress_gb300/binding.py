@@ -45,6 +45,8 @@ _SIGS = {
     "kpool_score_topk_workspace_size": (_SZ, [_L, _I, _I]),
     "kpool_score_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I, _I,
                               _P, _P, _P, _SZ, _P]),
+    "kpool_score_topk_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I,
+                                      _I, _P, _P, _P]),
     "kpool_score_dense": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I,
                                _P, _P, _SZ, _P]),
     "kpool_expand_indices": (_I, [_P, _P, _P, _I, _L, _I, _I, _I, _P, _P]),
@@ -211,6 +213,26 @@ def kpool_score_topk(q, w, pk, kpool: int, index_topk: int, cu_seqlens=None, cu_
                                  _ptr(cu_seqlens), _ptr(cu_pools), n_docs, T, P, H, D, kpool,
                                  index_topk, int(fp8), _ptr(idx), _ptr(sc), _ptr(workspace),
                                  workspace.numel(), _stream(q.device)), "kpool_score_topk")
+    return idx, sc
+
+
+def kpool_score_topk_noalloc(q, w, pk, kpool: int, index_topk: int, cu_seqlens=None,
+                             cu_pools=None, q_scale=None, pk_scale=None, out=None):
+    """kpool_score_topk without a workspace: the library's fixed scratch
+    array stands in for it (see include/kpool.h for its limits)."""
+    fp8, n_docs, T, H, D, P = _score_common(q, w, pk, q_scale, pk_scale, cu_seqlens, cu_pools)
+    Kp = index_topk // kpool
+    if out is None:
+        idx = torch.empty(T, Kp, dtype=torch.int32, device=q.device)
+        sc = torch.empty(T, Kp, dtype=torch.float32, device=q.device)
+    else:
+        idx, sc = out
+    _check(_lib.kpool_score_topk_noalloc(_ptr(_as_u8(q)) if fp8 else _ptr(q), _ptr(q_scale),
+                                         _ptr(w), _ptr(_as_u8(pk)) if fp8 else _ptr(pk),
+                                         _ptr(pk_scale), _ptr(cu_seqlens), _ptr(cu_pools), n_docs,
+                                         T, P, H, D, kpool, index_topk, int(fp8), _ptr(idx),
+                                         _ptr(sc), _stream(q.device)),
+           "kpool_score_topk_noalloc")
     return idx, sc
 
 

@@ -248,6 +248,39 @@ int kpool_score_topk(const void *q, const float *q_scale, const float *w, const 
     return run_score(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kpool_score_topk_noalloc(const void *q, const float *q_scale, const float *w, const void *pk,
+                             const float *pk_scale, const int32_t *cu_seqlens,
+                             const int32_t *cu_pools, int n_docs, int64_t T, int64_t P_total,
+                             int H, int D, int kpool, int index_topk, int fp8,
+                             int32_t *pool_idx_out, float *pool_score_out, kpool_stream_t stream)
+{
+    clear_error();
+    int rc = check_common(T, kpool);
+    if (rc) return rc;
+    if ((rc = check_h(H))) return rc;
+    if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1 (got %d)", n_docs);
+    int *scratch = nullptr;
+    size_t scratch_bytes = 0;
+    int64_t max_tiles = 0;
+    const int64_t QT = 256 / H;
+    const int64_t need_tiles = (T + QT - 1) / QT + n_docs;
+    // the capacity is a compile-time constant: reject before touching the device
+    if (need_tiles > kNoAllocMaxTiles)
+        return fail(KPOOL_ERR_UNSUPPORTED,
+                    "kpool_score_topk_noalloc: T=%lld with H=%d and %d documents needs %lld "
+                    "query tiles; its fixed scratch holds at most %d (use kpool_score_topk "
+                    "with a caller-provided workspace)",
+                    static_cast<long long>(T), H, n_docs, static_cast<long long>(need_tiles),
+                    kNoAllocMaxTiles);
+    if ((rc = noalloc_scratch(&scratch, &scratch_bytes, &max_tiles))) return rc;
+    if (need_tiles > max_tiles)
+        return fail(KPOOL_ERR_UNSUPPORTED, "no-alloc scratch too small (%lld tiles needed)",
+                    static_cast<long long>(need_tiles));
+    return kpool_score_topk(q, q_scale, w, pk, pk_scale, cu_seqlens, cu_pools, n_docs, T, P_total,
+                            H, D, kpool, index_topk, fp8, pool_idx_out, pool_score_out, scratch,
+                            scratch_bytes, stream);
+}
+
 int kpool_score_dense(const void *q, const float *q_scale, const float *w, const void *pk,
                       const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
                       int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool, int fp8,

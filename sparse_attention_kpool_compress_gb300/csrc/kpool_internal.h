@@ -68,5 +68,10 @@ struct ScoreArgs {
 size_t score_workspace_bytes(int64_t T, int H, int n_docs);
 int score_capacity(int H, int D, int fp8);   // candidate slots per query (0 = unsupported)
 int run_score(const ScoreArgs &a, cudaStream_t s);
+// Query tiles the fixed scratch of kpool_score_topk_noalloc can schedule.
+constexpr int kNoAllocMaxTiles = 131072;
+// Device address, size and tile capacity of the no-alloc scratch array of
+// the current device (looked up on first use per device).
+int noalloc_scratch(int **ptr, size_t *bytes, int64_t *max_tiles);
 
 }  // namespace kpool

@@ -27,6 +27,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kpool_internal.h"
 #include "kpool_ptx.cuh"
@@ -784,7 +785,39 @@ int launch_h(const ScoreArgs &a, const Layout &L, const CUtensorMap &mq, const C
     return KPOOL_OK;
 }
 
+// Scratch of the allocation-free entry point (kpool_score_topk_noalloc): the
+// workspace header and the query-tile table for up to kNoAllocMaxTiles tiles,
+// 1 MiB + 256 B, held by every device that loads the library.  The schedule
+// kernel rewrites the counter, status word, tile count and table on every
+// call, so no state from an earlier call is read.
+constexpr size_t kNoAllocWords = WS_TABLE_INTS + 2 * static_cast<size_t>(kNoAllocMaxTiles);
+static __device__ __align__(256) int g_noalloc_scratch[kNoAllocWords];
+
 }  // namespace
+
+int noalloc_scratch(int **ptr, size_t *bytes, int64_t *max_tiles)
+{
+    static std::mutex mu;
+    static std::vector<int *> addr;   // device address of the scratch, per device
+    int dev = 0;
+    KPOOL_CUDA_CHECK(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(mu);
+    if (static_cast<int>(addr.size()) <= dev) addr.resize(dev + 1, nullptr);
+    if (addr[dev] == nullptr) {
+        // The array's name is a host-side stand-in; the kernel needs the device
+        // address, looked up once per device with that device current.
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(KPOOL_ERR_CUDA, "cudaGetSymbolAddress(no-alloc scratch) failed: %s",
+                        cudaGetErrorString(e));
+        addr[dev] = static_cast<int *>(p);
+    }
+    *ptr = addr[dev];
+    *bytes = kNoAllocWords * sizeof(int);
+    *max_tiles = kNoAllocMaxTiles;
+    return KPOOL_OK;
+}
 
 size_t score_workspace_bytes(int64_t T, int H, int n_docs)
 {
