@@ -33,15 +33,22 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
+    """variant "" builds libkpool.so; "phase_timers" builds libkpool_phase_timers.so with
+    -DKPOOL_PHASE_TIMERS (per-phase cycle counters of the scoring kernel)."""
+    build_dir, lib_path = BUILD, LIB
+    if variant:
+        extra_flags = tuple(extra_flags) + ("-DKPOOL_%s" % variant.upper(),)
+        build_dir = os.path.join(HERE, "_build_" + variant)
+        lib_path = os.path.join(HERE, "libkpool_%s.so" % variant)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     hdrs = [os.path.join(CSRC, h) for h in HEADERS]
     hdrs.append(os.path.join(os.path.dirname(HERE), "include", "kpool.h"))
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         if force or _stale(o, [s] + hdrs):
             cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", s, "-o", o]
             if verbose:
@@ -55,15 +62,19 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp%d" % os.getpid()
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    var = ""
+    for a in sys.argv[1:]:
+        if a.startswith("--variant="):
+            var = a.split("=", 1)[1]
+    print(build(force="--force" in sys.argv, verbose=True, variant=var))

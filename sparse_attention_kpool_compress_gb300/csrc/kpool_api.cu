@@ -232,9 +232,12 @@ int kpool_score_topk(const void *q, const float *q_scale, const float *w, const 
         return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
     const int Kp = index_topk / kpool;
     const int cap = score_capacity(H, D, fp8);
-    if (Kp + 128 > cap)
+    int kp2 = 1;
+    while (kp2 < Kp) kp2 <<= 1;
+    if (Kp + 128 > cap || kp2 > cap)
         return fail(KPOOL_ERR_UNSUPPORTED,
-                    "index_topk / kpool = %d exceeds the per-query capacity %d - 128 for H=%d",
+                    "index_topk / kpool = %d exceeds the per-query candidate capacity %d for H=%d "
+                    "(needs Kp + 128 and the next power of two of Kp to fit)",
                     Kp, cap, H);
     if (T > 0 && (!pool_idx_out || !pool_score_out))
         return fail(KPOOL_ERR_INVALID_ARG, "pool_idx_out and pool_score_out must be non-NULL");

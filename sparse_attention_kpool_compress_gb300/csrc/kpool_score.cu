@@ -44,10 +44,38 @@ constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
 constexpr int kSmemLimit = 232448;                    // 227 KiB per block (opt-in max)
 constexpr int kMaxC = 4096;
-constexpr int kMaxR = kMaxC / kEpiThreads;            // 16 entries per thread in a compaction
-constexpr int kMaxStages = 6;
 constexpr uint64_t kTimeoutNs = 2000000000ull;        // 2 s per wait
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr int kGroups = 4;                            // selection groups of the epilogue
+constexpr int kGroupWarps = kEpiWarps / kGroups;      // 2 warps per group
+constexpr int kGroupThreads = 32 * kGroupWarps;       // 64
+constexpr int kSlack = 64;                            // extra entries a mid-stream prune may keep
+// register split (setmaxnreg): 128 threads x 56 + 256 x 224 = 384 x 168
+constexpr int kRegsOther = 56, kRegsEpi = 224;
+
+// Optional phase timers (build with -DKPOOL_PHASE_TIMERS): per-role cycle
+// counts of waits and work, summed over all CTAs into g_phase_timers and read
+// back with kpool_debug_phase_timers.  Compiled out by default.
+#ifdef KPOOL_PHASE_TIMERS
+__device__ unsigned long long g_phase_timers[32];
+#define PT_DECL                                \
+    unsigned long long pt_[8] = {};            \
+    unsigned long long pt_t = clock64();
+#define PT_MARK(i)                             \
+    do {                                       \
+        const unsigned long long n_ = clock64(); \
+        pt_[i] += n_ - pt_t;                   \
+        pt_t = n_;                             \
+    } while (0)
+#define PT_FLUSH(base)                                                       \
+    do {                                                                     \
+        for (int i_ = 0; i_ < 8; ++i_) atomicAdd(&g_phase_timers[(base) + i_], pt_[i_]); \
+    } while (0)
+#else
+#define PT_DECL
+#define PT_MARK(i) do {} while (0)
+#define PT_FLUSH(base) do {} while (0)
+#endif
 
 // barrier indices
 constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BTM_FULL = 2, BTM_EMPTY = 4, BTI_FULL = 6,
@@ -82,10 +110,10 @@ Layout make_layout(int H, int D, int fp8)
     L.pk_off = L.q_off + L.n_kchunks * L.q_chunk;
     L.pk_stage = L.n_kchunks * L.pk_chunk;
     uint32_t off = L.pk_off + L.stages * L.pk_stage;
-    L.ws_off = off;   off += kEpiWarps * 128 * 4;
-    L.hist_off = off; off += 256 * 4;
+    L.ws_off = off;   off += 0;   // head weights live in registers
+    L.hist_off = off; off += kGroups * 256 * 4;
     L.cnt_off = off;  off += 2 * QT * 4 * 4;
-    L.scr_off = off;  off += 64 * 4;
+    L.scr_off = off;  off += kGroups * 32 * 4 + ((QT * 4 + 15) / 16) * 16;
     L.thr_off = off;  off += ((QT * 4 + 15) / 16) * 16;
     L.bar_off = off;  off += 256;
     L.ti_off = off;   off += 2 * 16;
@@ -165,36 +193,68 @@ __device__ __forceinline__ int pool_tiles_of(const TileInfo &ti, int QT, int kp)
     return (nc_last + kBM - 1) / kBM;
 }
 
-// Keep the k best entries (score desc; earlier position wins ties) of
-// cs/ci[0..n), n > k, in place and in order.  All 256 epilogue threads.
-// Writes the threshold key to *thr_out.
-__device__ void select_topk(float *cs, int *ci, int n, int k, int etid, int *hist, int *scr,
-                            uint32_t *thr_out)
+__device__ __forceinline__ void group_bar(int g) { ptx::named_bar_sync(2 + g, kGroupThreads); }
+
+// Radix search (DeepSelect-style, 8-bit digits) for the k-th largest of
+// keyf(e) over the entries e < n with partf(e), by one group of 64 threads.
+// Digits start at the highest bit where the smallest and largest
+// participating key differ, so the first histogram is spread.  Results:
+//   kth    the k-th largest key, or (edge) the lower edge of the digit bin
+//          holding it when that bin is needed whole or, with allow_edge, when
+//          keeping everything at or above the edge keeps <= k + slack entries;
+//   above  participants with key above the bin / above kth;
+//   inbin  participants in that bin / equal to kth.
+template <class KeyFn, class PartFn>
+__device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, bool allow_edge,
+                          int slack, int g, int gtid, int *hist, int *gs, uint32_t &kth,
+                          int &above, int &inbin, bool &edge)
 {
-    const int lane = etid & 31, ew = etid >> 5;
-    uint32_t prefix = 0;
-    int kr = k;
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        hist[etid] = 0;
-        ptx::named_bar_sync(1, kEpiThreads);
-        for (int base = 0; base < n; base += kEpiThreads) {
-            const int e = base + etid;
-            uint32_t key = 0;
-            bool ok = false;
-            if (e < n) {
-                key = fkey(cs[e]);
-                ok = (pass == 0) || ((key >> (shift + 8)) == (prefix >> (shift + 8)));
-            }
-            const uint32_t digit = (key >> shift) & 255u;
-            const unsigned m = __ballot_sync(kFull, ok);
-            if (ok) {
-                const unsigned peers = __match_any_sync(m, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
-            }
+    const int lane = gtid & 31, gw = gtid >> 5;
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    int cnt = 0;
+    for (int e = gtid; e < n; e += kGroupThreads) {
+        if (partf(e)) {
+            const uint32_t key = keyf(e);
+            kmin = min(kmin, key);
+            kmax = max(kmax, key);
+            ++cnt;
         }
-        ptx::named_bar_sync(1, kEpiThreads);
-        if (ew == 0) {
+    }
+    kmin = __reduce_min_sync(kFull, kmin);
+    kmax = __reduce_max_sync(kFull, kmax);
+    cnt = __reduce_add_sync(kFull, cnt);
+    if (lane == 0) {
+        gs[gw] = static_cast<int>(kmin);
+        gs[2 + gw] = static_cast<int>(kmax);
+        gs[4 + gw] = cnt;
+    }
+    group_bar(g);
+    kmin = min(static_cast<uint32_t>(gs[0]), static_cast<uint32_t>(gs[1]));
+    kmax = max(static_cast<uint32_t>(gs[2]), static_cast<uint32_t>(gs[3]));
+    cnt = gs[4] + gs[5];
+    above = 0;
+    if (kmin == kmax) {
+        kth = kmax;
+        inbin = cnt;
+        edge = false;
+        return;
+    }
+    int hi = 31 - __clz(kmin ^ kmax);
+    uint32_t prefix = hi == 31 ? 0u : (kmax & ~((2u << hi) - 1u));
+    int kr = k;
+    while (true) {
+        const int lo = max(hi - 7, 0);
+        const uint32_t dmask = (2u << (hi - lo)) - 1u;
+        for (int i = gtid; i < 256; i += kGroupThreads) hist[i] = 0;
+        group_bar(g);
+        for (int e = gtid; e < n; e += kGroupThreads) {
+            if (!partf(e)) continue;
+            const uint32_t key = keyf(e);
+            if (hi == 31 || (key >> (hi + 1)) == (prefix >> (hi + 1)))
+                atomicAdd(&hist[(key >> lo) & dmask], 1);
+        }
+        group_bar(g);
+        if (gw == 0) {
             int b[8];
             int local = 0;
 #pragma unroll
@@ -208,82 +268,201 @@ __device__ void select_topk(float *cs, int *ci, int n, int k, int etid, int *his
                 const int o = __shfl_down_sync(kFull, suf, off);
                 if (lane + off < 32) suf += o;
             }
-            int cum = suf - local;   // entries in higher bins of higher lanes
+            int cum = suf - local;
 #pragma unroll
             for (int i = 7; i >= 0; --i) {
                 if (cum < kr && cum + b[i] >= kr) {
-                    scr[2 * pass] = lane * 8 + i;
-                    scr[2 * pass + 1] = cum;
+                    gs[8] = lane * 8 + i;
+                    gs[9] = cum;
+                    gs[10] = b[i];
                 }
                 cum += b[i];
             }
         }
-        ptx::named_bar_sync(1, kEpiThreads);
-        prefix |= static_cast<uint32_t>(scr[2 * pass]) << shift;
-        kr -= scr[2 * pass + 1];
+        group_bar(g);
+        const int d = gs[8], cum = gs[9], hb = gs[10];
+        prefix |= static_cast<uint32_t>(d) << lo;
+        kr -= cum;
+        above += cum;
+        if (hb == kr || (allow_edge && above + hb <= k + slack)) {
+            kth = prefix;
+            inbin = hb;
+            edge = true;
+            return;
+        }
+        if (lo == 0) {
+            kth = prefix;
+            inbin = hb;
+            edge = false;
+            return;
+        }
+        hi = lo - 1;
     }
-    const uint32_t kstar = prefix;
-    const int need = kr;   // entries equal to kstar to keep (the earliest ones)
-    const int R = (n + kEpiThreads - 1) / kEpiThreads;
+}
+
+// Keep the k best of cs/ci[0..n), n > k (score descending, equal scores by
+// lower pool index), in place, by one group of 64 epilogue threads.  In prune
+// mode (exact = false) it may keep up to k + slack entries: all those at or
+// above a digit-bin edge.  Returns the number kept and writes to *thr_out the
+// key a later candidate (higher pool index) must exceed to possibly enter.
+__device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int slack, int g,
+                            int gtid, int *hist, int *gs, uint32_t *thr_out)
+{
+    const int lane = gtid & 31, gw = gtid >> 5;
     const unsigned lt = (1u << lane) - 1u;
-    float sv[kMaxR];
-    int iv[kMaxR];
-    unsigned tb[kMaxR];
-    int nt = 0;
+    uint32_t kth;
+    int above, inbin;
+    bool edge;
+    radix_kth(n, k, [&](int e) { return fkey(cs[e]); }, [](int) { return true; }, !exact, slack, g,
+              gtid, hist, gs, kth, above, inbin, edge);
+    // ties at the k-th score: keep the lowest pool indices among them
+    uint32_t ithr = 0xFFFFFFFFu;   // keep tied entries with ci <= ithr
+    const bool ties = !edge && above + inbin > k;
+    if (ties) {
+        const int need = k - above;
+        uint32_t ik;
+        int iab, iin;
+        bool ied;
+        group_bar(g);   // gs reuse
+        radix_kth(n, need, [&](int e) { return ~static_cast<uint32_t>(ci[e]); },
+                  [&](int e) { return fkey(cs[e]) == kth; }, false, 0, g, gtid, hist, gs, ik, iab,
+                  iin, ied);
+        ithr = ~ik;
+    }
+    group_bar(g);   // gs reused below
+    const int chunks = (n + 31) / 32;
+    const int per = ((chunks + kGroupWarps - 1) / kGroupWarps) * 32;
+    const int r0 = gw * per, r1 = min(n, r0 + per);
+    int cnt = 0;
+    for (int c = r0; c < r1; c += 32) {
+        const int e = c + lane;
+        float sv = 0.f;
+        int iv = 0;
+        bool keep = false;
+        if (e < r1) {
+            sv = cs[e];
+            iv = ci[e];
+            const uint32_t key = fkey(sv);
+            keep = edge ? key >= kth
+                        : (key > kth || (key == kth && static_cast<uint32_t>(iv) <= ithr));
+        }
+        const unsigned kb = __ballot_sync(kFull, keep);
+        if (keep) {
+            const int dst = r0 + cnt + __popc(kb & lt);
+            cs[dst] = sv;
+            ci[dst] = iv;
+        }
+        cnt += __popc(kb);
+    }
+    if (lane == 0) gs[16 + gw] = cnt;
+    group_bar(g);
+    int total = 0, mybase = 0;
 #pragma unroll
-    for (int r = 0; r < kMaxR; ++r) {
-        tb[r] = 0;
-        sv[r] = 0.f;
-        iv[r] = 0;
-        if (r < R) {
-            const int e = ew * 32 * R + r * 32 + lane;
-            bool tie = false;
-            if (e < n) {
-                sv[r] = cs[e];
-                iv[r] = ci[e];
-                tie = fkey(sv[r]) == kstar;
+    for (int w = 0; w < kGroupWarps; ++w) {
+        if (w == gw) mybase = total;
+        total += gs[16 + w];
+    }
+    // move each later warp's kept block down behind the earlier ones, in order
+    for (int w = 1; w < kGroupWarps; ++w) {
+        if (gw == w) {
+            for (int c = 0; c < cnt; c += 32) {
+                const int i = c + lane;
+                float sv = 0.f;
+                int iv = 0;
+                if (i < cnt) {
+                    sv = cs[r0 + i];
+                    iv = ci[r0 + i];
+                }
+                __syncwarp();
+                if (i < cnt) {
+                    cs[mybase + i] = sv;
+                    ci[mybase + i] = iv;
+                }
             }
-            tb[r] = __ballot_sync(kFull, tie);
-            nt += __popc(tb[r]);
         }
+        group_bar(g);
     }
-    if (lane == 0) scr[8 + ew] = nt;
-    ptx::named_bar_sync(1, kEpiThreads);
-    int run = 0;
-    for (int w2 = 0; w2 < ew; ++w2) run += scr[8 + w2];
-    unsigned kb[kMaxR];
-    int nk = 0;
-#pragma unroll
-    for (int r = 0; r < kMaxR; ++r) {
-        kb[r] = 0;
-        if (r < R) {
-            const int e = ew * 32 * R + r * 32 + lane;
-            const uint32_t key = fkey(sv[r]);
-            const bool tie = (tb[r] >> lane) & 1u;
-            const int trank = run + __popc(tb[r] & lt);
-            const bool keep = (e < n) && (key > kstar || (tie && trank < need));
-            run += __popc(tb[r]);
-            kb[r] = __ballot_sync(kFull, keep);
-            nk += __popc(kb[r]);
-        }
+    if (gtid == 0) *thr_out = edge ? (kth > 0 ? kth - 1u : 0u) : kth;
+    group_bar(g);
+    return total;
+}
+
+// Write the n kept entries of cs/ci to out_idx/out_score in ascending pool
+// order by ranking them through a bitmap of the query's visible pools (local
+// index ci - pool_base < 32 * words).  The bitmap lives in ci[n .. n+words)
+// and the per-word prefix counts in cs[n .. n+words) (the free tail of the
+// query's candidate area; words <= capacity - n).  One group.
+__device__ void group_rank_store(float *cs, int *ci, int n, int pool_base, int words, int g,
+                                 int gtid, int *gs, int32_t *out_idx, float *out_score)
+{
+    const int lane = gtid & 31, gw = gtid >> 5;
+    uint32_t *bm = reinterpret_cast<uint32_t *>(ci + n);
+    int *pf = reinterpret_cast<int *>(cs + n);
+    for (int w = gtid; w < words; w += kGroupThreads) bm[w] = 0u;
+    group_bar(g);
+    for (int e = gtid; e < n; e += kGroupThreads) {
+        const int j = ci[e] - pool_base;
+        atomicOr(&bm[j >> 5], 1u << (j & 31));
     }
-    if (lane == 0) scr[16 + ew] = nk;
-    ptx::named_bar_sync(1, kEpiThreads);
-    int pos = 0;
-    for (int w2 = 0; w2 < ew; ++w2) pos += scr[16 + w2];
+    group_bar(g);
+    // exclusive prefix of popcounts over words: each thread a contiguous run
+    const int per = (words + kGroupThreads - 1) / kGroupThreads;
+    const int w0 = gtid * per, w1 = min(words, w0 + per);
+    int local = 0;
+    for (int w = w0; w < w1; ++w) local += __popc(bm[w]);
+    int incl = local;
 #pragma unroll
-    for (int r = 0; r < kMaxR; ++r) {
-        if (r < R) {
-            if ((kb[r] >> lane) & 1u) {
-                const int d = pos + __popc(kb[r] & lt);
-                cs[d] = sv[r];
-                ci[d] = iv[r];
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) gs[20 + gw] = incl;
+    group_bar(g);
+    int run = incl - local;
+    for (int w = 0; w < gw; ++w) run += gs[20 + w];
+    for (int w = w0; w < w1; ++w) {
+        pf[w] = run;
+        run += __popc(bm[w]);
+    }
+    group_bar(g);
+    for (int e = gtid; e < n; e += kGroupThreads) {
+        const int j = ci[e] - pool_base;
+        const int r = pf[j >> 5] + __popc(bm[j >> 5] & ((1u << (j & 31)) - 1u));
+        out_idx[r] = ci[e];
+        out_score[r] = cs[e];
+    }
+}
+
+// Ascending sort of cs/ci[0..n) by pool index (ci), bitonic over the next
+// power of two (pad entries carry INT_MAX), by one group.  n2 <= capacity.
+__device__ void group_sort_by_pool(float *cs, int *ci, int n, int g, int gtid)
+{
+    int n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (int i = n + gtid; i < n2; i += kGroupThreads) {
+        ci[i] = 0x7FFFFFFF;
+        cs[i] = -INFINITY;
+    }
+    group_bar(g);
+    for (int kk = 2; kk <= n2; kk <<= 1) {
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            for (int i = gtid; i < n2; i += kGroupThreads) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const int a = ci[i], b = ci[ixj];
+                    const bool up = (i & kk) == 0;
+                    if ((a > b) == up) {
+                        ci[i] = b;
+                        ci[ixj] = a;
+                        const float t = cs[i];
+                        cs[i] = cs[ixj];
+                        cs[ixj] = t;
+                    }
+                }
             }
-            pos += __popc(kb[r]);
+            group_bar(g);
         }
     }
-    if (etid == 0) *thr_out = kstar;
-    ptx::named_bar_sync(1, kEpiThreads);
 }
 
 template <int H>
@@ -293,11 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     constexpr int QT = kBN / H;   // queries per tile
     constexpr int QW = QT / 2;    // queries per epilogue warp
-    constexpr int NSL = QT > 32 ? 2 : 1;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned base, derived by pointer arithmetic so that every pointer
+    // below stays a shared-memory pointer (LDS/STS/ATOMS, not generic accesses)
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const Layout &L = p.L;
     const uint32_t sbase = ptx::smem_u32(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
@@ -323,6 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(BPK_FULL + S + s), 1);
         }
         misc[1] = 0u;
+        int *qcnt0 = reinterpret_cast<int *>(smem + L.cnt_off);
+        uint32_t *thr0 = reinterpret_cast<uint32_t *>(smem + L.thr_off);
+        for (int q = 0; q < QT; ++q) {
+            qcnt0[q] = 0;
+            thr0[q] = 0u;
+        }
         ptx::fence_mbar_init();
     }
     if (warp == 2) {
@@ -351,9 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         return t;
     };
 
+    // registers: the producer/MMA/allocator warpgroup gives up most of its share
+    // to the two epilogue warpgroups (head weights stay in registers)
+    if (warp < 4) {
+    ptx::setmaxnreg_dec<kRegsOther>();
     if (warp == 0) {
         // ---------------- TMA producer + scheduler ----------------
         if (lane == 0) {
+            PT_DECL
             ptx::tma_prefetch_desc(&tm_q);
             ptx::tma_prefetch_desc(&tm_pk);
             const int ntiles = *reinterpret_cast<volatile int *>(p.ws + WS_NTILES);
@@ -366,7 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0;; ++it) {
                 const int slot = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
+                PT_MARK(4);
                 if (!wait_bar(bar(BTI_EMPTY + slot), tph ^ 1, sy)) break;
+                PT_MARK(0);
                 const int tile = atomicAdd(p.ws + WS_COUNTER, 1);
                 TileInfo t;
                 if (tile >= ntiles) {
@@ -380,7 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t.t0 < 0) break;
                 const int npt = pool_tiles_of(t, QT, p.kp);
                 if (npt == 0) continue;
+                PT_MARK(4);
                 if (!wait_bar(bar(BQ_EMPTY), qe_ph ^ 1, sy)) break;
+                PT_MARK(1);
                 qe_ph ^= 1;
                 ptx::mbar_arrive_expect_tx(bar(BQ_FULL), p.q_tx);
                 for (int c = 0; c < L.n_kchunks; ++c)
@@ -390,7 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 q_issued_ph = qe_ph ^ 1;
                 bool ok = true;
                 for (int i = 0; i < npt; ++i) {
+                    PT_MARK(3);
                     if (!wait_bar(bar(BPK_FULL + S + stage), ph ^ 1, sy)) { ok = false; break; }
+                    PT_MARK(2);
                     ptx::mbar_arrive_expect_tx(bar(BPK_FULL + stage), p.pk_tx);
                     const uint32_t dst = sbase + L.pk_off + stage * L.pk_stage;
                     for (int c = 0; c < L.n_kchunks; ++c)
@@ -414,28 +610,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (!ptx::mbar_try_wait(bar(BQ_FULL), q_issued_ph))
                     if (ptx::globaltimer() - t0 > kTimeoutNs) break;
             }
+            PT_MARK(4);
+            PT_FLUSH(16);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
+            PT_DECL
             int stage = 0, acc = 0;
             uint32_t ph = 0, qf_ph = 0, acc_ph = 0;
             bool any = false;
             for (int it = 0;; ++it) {
                 const int slot = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
+                PT_MARK(5);
                 if (!wait_bar(bar(BTI_FULL + slot), tph, sy)) break;
+                PT_MARK(0);
                 const TileInfo t = ti_slots[slot];   // after the acquiring wait
                 ptx::mbar_arrive(bar(BTI_EMPTY + slot));
                 if (t.t0 < 0) break;
                 const int npt = pool_tiles_of(t, QT, p.kp);
                 if (npt == 0) continue;
+                PT_MARK(5);
                 if (!wait_bar(bar(BQ_FULL), qf_ph, sy)) break;
+                PT_MARK(1);
                 qf_ph ^= 1;
                 bool ok = true;
                 for (int i = 0; i < npt; ++i) {
+                    PT_MARK(4);
                     if (!wait_bar(bar(BTM_EMPTY + acc), acc_ph ^ 1, sy)) { ok = false; break; }
+                    PT_MARK(2);
                     if (!wait_bar(bar(BPK_FULL + stage), ph, sy)) { ok = false; break; }
+                    PT_MARK(3);
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * kAccCols;
                     const uint32_t a0 = sbase + L.pk_off + stage * L.pk_stage;
@@ -466,29 +672,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (!ptx::mbar_try_wait(bar(BDRAIN), 0))
                     if (ptx::globaltimer() - t0 > kTimeoutNs) break;
             }
+            PT_MARK(5);
+            PT_FLUSH(8);
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        ptx::setmaxnreg_inc<kRegsEpi>();
         // ---------------- epilogue ----------------
+        constexpr int NACC = H >= 32 ? 4 : (H >= 16 ? 2 : 1);   // FFMA2 chains per query
         const int ew = warp - 4;
         const int qr = warp & 3;            // TMEM lane quarter
         const int hf = ew >> 2;             // which half of the 256 columns
         const int etid = threadIdx.x - 128;
-        float *ws = reinterpret_cast<float *>(smem + L.ws_off) + ew * 128;
-        int *hist = reinterpret_cast<int *>(smem + L.hist_off);
-        int *cnts = reinterpret_cast<int *>(smem + L.cnt_off);
-        int *scr = reinterpret_cast<int *>(smem + L.scr_off);
+        const int g = ew / kGroupWarps;     // selection group
+        const int gtid = etid - g * kGroupThreads;
+        int *hist = reinterpret_cast<int *>(smem + L.hist_off) + g * 256;
+        int *gs = reinterpret_cast<int *>(smem + L.scr_off) + g * 32;
+        int *qcnt = reinterpret_cast<int *>(smem + L.cnt_off);   // candidates per query
         uint32_t *thr_s = reinterpret_cast<uint32_t *>(smem + L.thr_off);
         float *cs = reinterpret_cast<float *>(smem + L.cs_off);
         int *ci = reinterpret_cast<int *>(smem + L.ci_off);
         const int C = L.C;
         const int Kp = p.Kp;
+        const int slack = max(0, min(kSlack, C - kBM - Kp));
+        // tiles between capacity checks; a query above `room` candidates at a
+        // check is compacted, so the next G tiles (<= 128 each) always fit
+        const int G = max(1, min(4, (C - Kp - slack) / kBM));
+        const int room = C - G * kBM;
         const unsigned lt = (1u << lane) - 1u;
-        int acc = 0, tile_seq = 0;
+        int acc = 0;
         uint32_t acc_ph = 0;
+        PT_DECL
         for (int it = 0;; ++it) {
             const int slot = it & 1;
             const uint32_t tph = (it >> 1) & 1;
+            PT_MARK(7);
             if (!wait_bar_warp(bar(BTI_FULL + slot), tph, sy)) break;
+            PT_MARK(0);
             const TileInfo t = ti_slots[slot];
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(BTI_EMPTY + slot));
@@ -497,24 +717,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nq = min(QT, t.doc_end - t.t0);
             const int npt = pool_tiles_of(t, QT, p.kp);
 
-            // this warp's head weights (128 contiguous floats), w * q_scale in FP8 mode
-            __syncwarp();
+            // this warp's 128 head weights (w, times q_scale in FP8 mode), held in
+            // registers as packed pairs for the whole query tile
+            uint64_t w2[64];
             {
-                const int c0 = lane * 4;
-                const int qi = hf * QW + c0 / H;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (qi < nq) {
-                    const int64_t off = static_cast<int64_t>(t.t0 + hf * QW) * H + c0;
-                    v = *reinterpret_cast<const float4 *>(p.w + off);
-                    if (p.fp8) {
-                        const float4 s4 = *reinterpret_cast<const float4 *>(p.q_scale + off);
-                        v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
+                const int64_t base = static_cast<int64_t>(t.t0 + hf * QW) * H;
+#pragma unroll
+                for (int c = 0; c < 128; c += 4) {
+                    const int qi = hf * QW + c / H;
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (qi < nq) {
+                        v = __ldg(reinterpret_cast<const float4 *>(p.w + base + c));
+                        if (p.fp8) {
+                            const float4 s4 =
+                                __ldg(reinterpret_cast<const float4 *>(p.q_scale + base + c));
+                            v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
+                        }
                     }
+                    w2[c / 2] = ptx::pack_f32x2(v.x, v.y);
+                    w2[c / 2 + 1] = ptx::pack_f32x2(v.z, v.w);
                 }
-                *reinterpret_cast<float4 *>(ws + c0) = v;
             }
-            __syncwarp();
-            const float4 *ws4 = reinterpret_cast<const float4 *>(ws);
 
             uint32_t thr[QW];
             int nc[QW];
@@ -523,46 +746,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 thr[j] = 0u;
                 nc[j] = (tau0 + hf * QW + j + 1) / p.kp;
             }
-            int tot[NSL];
-#pragma unroll
-            for (int sl = 0; sl < NSL; ++sl) tot[sl] = 0;
-            if (etid < QT) thr_s[etid] = 0u;
             bool aborted = false;
 
             for (int i = 0; i < npt; ++i) {
+                PT_MARK(1);
                 if (!wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy)) { aborted = true; break; }
+                PT_MARK(2);
                 ptx::tc_fence_after();
                 const uint32_t tb = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) +
                                     acc * kAccCols + hf * 128;
-                float a0[QW], a1[QW];
+                uint64_t a4[QW][NACC];
 #pragma unroll
-                for (int j = 0; j < QW; ++j) { a0[j] = 0.f; a1[j] = 0.f; }
+                for (int j = 0; j < QW; ++j)
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v0[32], v1[32];
-                    ptx::tmem_ld32(tb + half * 64, v0);
-                    ptx::tmem_ld32(tb + half * 64 + 32, v1);
-                    ptx::tmem_ld_wait();
-                    if (half == 1) {
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
+                    for (int k = 0; k < NACC; ++k) a4[j][k] = 0ull;
+                // relu(x) * w summed per query: 4 chunks of 32 columns, the load
+                // of the next chunk overlapping the math on the current one
+                auto accum = [&](const uint32_t(&v)[32], const int c0) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 2) {
+                        const int col = c0 + x;
+                        const int j = col / H;
+                        const int k = (col / 2) % NACC;
+                        const uint64_t r = ptx::pack_f32x2(fmaxf(__uint_as_float(v[x]), 0.f),
+                                                           fmaxf(__uint_as_float(v[x + 1]), 0.f));
+                        a4[j][k] = ptx::ffma2(r, w2[col / 2], a4[j][k]);
                     }
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const uint32_t *v = cc ? v1 : v0;
-#pragma unroll
-                        for (int x = 0; x < 32; x += 4) {
-                            const int col = half * 64 + cc * 32 + x;
-                            const int j = col / H;
-                            const float4 w4 = ws4[col >> 2];
-                            a0[j] = fmaf(fmaxf(__uint_as_float(v[x + 0]), 0.f), w4.x, a0[j]);
-                            a1[j] = fmaf(fmaxf(__uint_as_float(v[x + 1]), 0.f), w4.y, a1[j]);
-                            a0[j] = fmaf(fmaxf(__uint_as_float(v[x + 2]), 0.f), w4.z, a0[j]);
-                            a1[j] = fmaf(fmaxf(__uint_as_float(v[x + 3]), 0.f), w4.w, a1[j]);
-                        }
-                    }
-                }
+                };
+                uint32_t va[32], vb[32];
+                ptx::tmem_ld32(tb, va);
+                ptx::tmem_ld_wait(va);
+                ptx::tmem_ld32(tb + 32, vb);
+                accum(va, 0);
+                ptx::tmem_ld_wait(vb);
+                ptx::tmem_ld32(tb + 64, va);
+                accum(vb, 32);
+                ptx::tmem_ld_wait(va);
+                ptx::tmem_ld32(tb + 96, vb);
+                accum(va, 64);
+                ptx::tmem_ld_wait(vb);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
+                accum(vb, 96);
                 if (++acc == 2) { acc = 0; acc_ph ^= 1; }
 
                 const int pool_local = i * kBM + qr * 32 + lane;
@@ -572,10 +798,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s[QW];
 #pragma unroll
                 for (int j = 0; j < QW; ++j) {
-                    float v = a0[j] + a1[j];
+                    float v = ptx::sum_f32x2(a4[j][0]);
+#pragma unroll
+                    for (int k = 1; k < NACC; ++k) v += ptx::sum_f32x2(a4[j][k]);
                     if (p.fp8) v *= sk;
                     s[j] = (v == 0.f) ? 0.f : v;   // fold -0 into +0
                 }
+                PT_MARK(3);
 
                 if (p.mode == 1) {   // dense scores (test/debug)
 #pragma unroll
@@ -587,80 +816,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
 
-                // ordered append of survivors of the threshold filter
-                const int par = (tile_seq & 1) * QT * 4;
-                ++tile_seq;
-                unsigned bal[QW];
+                // survivors of the threshold filter, appended (unordered) with one
+                // shared-memory atomic per warp and query that has any
 #pragma unroll
                 for (int j = 0; j < QW; ++j) {
                     const int qi = hf * QW + j;
                     const bool ps = (qi < nq) && (pool_local < nc[j]) && (fkey(s[j]) > thr[j]);
-                    bal[j] = __ballot_sync(kFull, ps);
-                    if (lane == 0) cnts[par + qi * 4 + qr] = __popc(bal[j]);
-                }
-                ptx::named_bar_sync(1, kEpiThreads);
-#pragma unroll
-                for (int j = 0; j < QW; ++j) {
-                    const int qi = hf * QW + j;
-                    const int4 c4 = *reinterpret_cast<const int4 *>(&cnts[par + qi * 4]);
-                    const int tq = __shfl_sync(kFull, (NSL > 1 && qi >= 32) ? tot[NSL - 1] : tot[0],
-                                               qi & 31);
-                    const int pre = (qr > 0 ? c4.x : 0) + (qr > 1 ? c4.y : 0) + (qr > 2 ? c4.z : 0);
-                    if ((bal[j] >> lane) & 1u) {
-                        const int d = qi * C + tq + pre + __popc(bal[j] & lt);
-                        cs[d] = s[j];
-                        ci[d] = pool_g;
-                    }
-                }
-                bool over = false;
-#pragma unroll
-                for (int sl = 0; sl < NSL; ++sl) {
-                    const int qi = lane + 32 * sl;
-                    if (qi < QT) {
-                        const int4 c4 = *reinterpret_cast<const int4 *>(&cnts[par + qi * 4]);
-                        tot[sl] += c4.x + c4.y + c4.z + c4.w;
-                        over |= tot[sl] > C - kBM;
-                    }
-                }
-                if (__any_sync(kFull, over)) {
-                    ptx::named_bar_sync(1, kEpiThreads);
-                    for (int qi = 0; qi < QT; ++qi) {
-                        const int sl = qi >> 5;
-                        const int tq = __shfl_sync(kFull, sl ? tot[NSL - 1] : tot[0], qi & 31);
-                        if (tq > C - kBM) {
-                            select_topk(cs + qi * C, ci + qi * C, tq, Kp, etid, hist, scr,
-                                        &thr_s[qi]);
-                            if (lane == (qi & 31)) {
-                                if (sl) tot[NSL - 1] = Kp;
-                                else tot[0] = Kp;
-                            }
+                    const unsigned bal = __ballot_sync(kFull, ps);
+                    if (bal != 0u) {
+                        int base = 0;
+                        if (lane == 0) base = atomicAdd(&qcnt[qi], __popc(bal));
+                        base = __shfl_sync(kFull, base, 0);
+                        if (ps) {
+                            const int d = qi * C + base + __popc(bal & lt);
+                            cs[d] = s[j];
+                            ci[d] = pool_g;
                         }
                     }
+                }
+                PT_MARK(4);
+                if ((i % G) == G - 1 && i != npt - 1) {
+                    // capacity check: compact queries past the room, plus those past
+                    // half of it, each group on its own queries in parallel
+                    ptx::named_bar_sync(1, kEpiThreads);
+                    bool over = false;
+                    for (int q = lane; q < QT; q += 32) over |= qcnt[q] > room;
+                    if (__any_sync(kFull, over)) {
+                        for (int q = g; q < QT; q += kGroups) {
+                            const int n = qcnt[q];
+                            if (n > (room + Kp) / 2) {
+                                const int nn = group_select(cs + q * C, ci + q * C, n, Kp, false,
+                                                            slack, g, gtid, hist, gs, &thr_s[q]);
+                                if (gtid == 0) qcnt[q] = nn;
+                            }
+                        }
+                        ptx::named_bar_sync(1, kEpiThreads);
 #pragma unroll
-                    for (int j = 0; j < QW; ++j) thr[j] = thr_s[hf * QW + j];
+                        for (int j = 0; j < QW; ++j) thr[j] = thr_s[hf * QW + j];
+                    }
+                    PT_MARK(5);
                 }
             }
             if (aborted) break;
             if (p.mode == 1) continue;
 
-            // final selection and output, one query at a time
+            // final selection, pool order and output: every group on its own queries
+            PT_MARK(1);
             ptx::named_bar_sync(1, kEpiThreads);
-            for (int qi = 0; qi < nq; ++qi) {
-                const int sl = qi >> 5;
-                int tq = __shfl_sync(kFull, sl ? tot[NSL - 1] : tot[0], qi & 31);
-                if (tq > Kp) {
-                    select_topk(cs + qi * C, ci + qi * C, tq, Kp, etid, hist, scr, &thr_s[qi]);
-                    tq = Kp;
+            for (int q = g; q < nq; q += kGroups) {
+                int n = qcnt[q];
+                float *csq = cs + q * C;
+                int *ciq = ci + q * C;
+                if (n > Kp) {
+                    group_select(csq, ciq, n, Kp, true, 0, g, gtid, hist, gs, &thr_s[q]);
+                    n = Kp;
                 }
-                const int64_t row = static_cast<int64_t>(t.t0 + qi) * Kp;
-                for (int e = etid; e < Kp; e += kEpiThreads) {
-                    const bool v = e < tq;
-                    p.pool_idx[row + e] = v ? ci[qi * C + e] : -1;
-                    p.pool_score[row + e] = v ? cs[qi * C + e] : -INFINITY;
+                const int64_t row = static_cast<int64_t>(t.t0 + q) * Kp;
+                const int nc_q = (tau0 + q + 1) / p.kp;   // local pools visible to q
+                const int words = (nc_q + 31) / 32;
+                if (words <= C - n) {
+                    group_rank_store(csq, ciq, n, t.pool_base, words, g, gtid, gs,
+                                     p.pool_idx + row, p.pool_score + row);
+                } else {
+                    group_sort_by_pool(csq, ciq, n, g, gtid);
+                    for (int e = gtid; e < n; e += kGroupThreads) {
+                        p.pool_idx[row + e] = ciq[e];
+                        p.pool_score[row + e] = csq[e];
+                    }
+                }
+                for (int e = n + gtid; e < Kp; e += kGroupThreads) {
+                    p.pool_idx[row + e] = -1;
+                    p.pool_score[row + e] = -INFINITY;
+                }
+            }
+            group_bar(g);
+            for (int q = g; q < QT; q += kGroups) {
+                if (gtid == 0) {
+                    qcnt[q] = 0;
+                    thr_s[q] = 0u;
                 }
             }
             ptx::named_bar_sync(1, kEpiThreads);
+            PT_MARK(6);
         }
+        PT_MARK(7);
+        if (lane == 0) PT_FLUSH(24);
     }
 
     __syncthreads();
@@ -677,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void schedule_kernel(const int32_t *cu, int n_docs, int T, int QT, int max_tiles,
                                 int *ws)
 {
-    __shared__ int s_ok, s_ntiles;
+    __shared__ int s_ntiles;
     if (threadIdx.x == 0) {
         int ok = 1, nt = 0;
         if (cu != nullptr) {
@@ -691,7 +931,6 @@ __global__ void schedule_kernel(const int32_t *cu, int n_docs, int T, int QT, in
             nt = (T + QT - 1) / QT;
         }
         if (nt > max_tiles) ok = 0;
-        s_ok = ok;
         s_ntiles = ok ? nt : 0;
         ws[WS_COUNTER] = 0;
         ws[WS_STATUS] = ok ? 0 : KPOOL_STATUS_BAD_SEQLENS;
@@ -818,6 +1057,19 @@ int noalloc_scratch(int **ptr, size_t *bytes, int64_t *max_tiles)
     *max_tiles = kNoAllocMaxTiles;
     return KPOOL_OK;
 }
+
+#ifdef KPOOL_PHASE_TIMERS
+extern "C" KPOOL_API int kpool_debug_phase_timers(unsigned long long *out32, int reset)
+{
+    KPOOL_CUDA_CHECK(cudaDeviceSynchronize());
+    KPOOL_CUDA_CHECK(cudaMemcpyFromSymbol(out32, g_phase_timers, 32 * sizeof(unsigned long long)));
+    if (reset) {
+        static const unsigned long long zero[32] = {};
+        KPOOL_CUDA_CHECK(cudaMemcpyToSymbol(g_phase_timers, zero, sizeof zero));
+    }
+    return KPOOL_OK;
+}
+#endif
 
 size_t score_workspace_bytes(int64_t T, int H, int n_docs)
 {
