@@ -110,7 +110,7 @@ Layout make_layout(int H, int D, int fp8)
     L.pk_off = L.q_off + L.n_kchunks * L.q_chunk;
     L.pk_stage = L.n_kchunks * L.pk_chunk;
     uint32_t off = L.pk_off + L.stages * L.pk_stage;
-    L.ws_off = off;   off += 0;   // head weights live in registers
+    L.ws_off = off;   off += kEpiWarps * 128 * 4;   // head weights of each epilogue warp
     L.hist_off = off; off += kGroups * 256 * 4;
     L.cnt_off = off;  off += 2 * QT * 4 * 4;
     L.scr_off = off;  off += kGroups * 32 * 4 + ((QT * 4 + 15) / 16) * 16;
@@ -644,16 +644,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     PT_MARK(3);
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * kAccCols;
-                    const uint32_t a0 = sbase + L.pk_off + stage * L.pk_stage;
-                    const uint32_t b0 = sbase + L.q_off;
-                    for (int c = 0; c < L.n_kchunks; ++c) {
+                    // descriptors of the K slices: the start-address field advances by
+                    // 32 bytes per MMA inside a 128-byte swizzled row, by a chunk
+                    // between 128-byte K chunks
+                    const uint64_t ad0 = ptx::smem_desc_sw128(sbase + L.pk_off + stage * L.pk_stage);
+                    const uint64_t bd0 = ptx::smem_desc_sw128(sbase + L.q_off);
+                    if (p.fp8) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = ptx::smem_desc_sw128(a0 + c * L.pk_chunk + kk * 32);
-                            const uint64_t bd = ptx::smem_desc_sw128(b0 + c * L.q_chunk + kk * 32);
-                            const uint32_t accum = (c | kk) != 0;
-                            if (p.fp8) ptx::mma_fp8(d_tmem, ad, bd, p.idesc, accum);
-                            else ptx::mma_bf16(d_tmem, ad, bd, p.idesc, accum);
+                        for (int kk = 0; kk < 4; ++kk)
+                            ptx::mma_fp8(d_tmem, ad0 + kk * 2, bd0 + kk * 2, p.idesc, kk != 0);
+                    } else {
+                        for (int c = 0; c < L.n_kchunks; ++c) {
+                            const uint64_t ad = ad0 + ((c * L.pk_chunk) >> 4);
+                            const uint64_t bd = bd0 + ((c * L.q_chunk) >> 4);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                ptx::mma_bf16(d_tmem, ad + kk * 2, bd + kk * 2, p.idesc,
+                                              (c | kk) != 0);
                         }
                     }
                     ptx::mma_commit(bar(BPK_FULL + S + stage));
@@ -717,27 +724,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nq = min(QT, t.doc_end - t.t0);
             const int npt = pool_tiles_of(t, QT, p.kp);
 
-            // this warp's 128 head weights (w, times q_scale in FP8 mode), held in
-            // registers as packed pairs for the whole query tile
-            uint64_t w2[64];
+            // this warp's 128 head weights (w, times q_scale in FP8 mode), staged in
+            // shared memory once per query tile and read back as broadcasts
+            float *wsm = reinterpret_cast<float *>(smem + L.ws_off) + ew * 128;
+            __syncwarp();
             {
-                const int64_t base = static_cast<int64_t>(t.t0 + hf * QW) * H;
-#pragma unroll
-                for (int c = 0; c < 128; c += 4) {
-                    const int qi = hf * QW + c / H;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (qi < nq) {
-                        v = __ldg(reinterpret_cast<const float4 *>(p.w + base + c));
-                        if (p.fp8) {
-                            const float4 s4 =
-                                __ldg(reinterpret_cast<const float4 *>(p.q_scale + base + c));
-                            v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
-                        }
+                const int c = lane * 4;
+                const int qi = hf * QW + c / H;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (qi < nq) {
+                    const int64_t off = static_cast<int64_t>(t.t0 + hf * QW) * H + c;
+                    v = __ldg(reinterpret_cast<const float4 *>(p.w + off));
+                    if (p.fp8) {
+                        const float4 s4 = __ldg(reinterpret_cast<const float4 *>(p.q_scale + off));
+                        v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
                     }
-                    w2[c / 2] = ptx::pack_f32x2(v.x, v.y);
-                    w2[c / 2 + 1] = ptx::pack_f32x2(v.z, v.w);
                 }
+                *reinterpret_cast<float4 *>(wsm + c) = v;
             }
+            __syncwarp();
+            const ulonglong2 *w4 = reinterpret_cast<const ulonglong2 *>(wsm);
 
             uint32_t thr[QW];
             int nc[QW];
@@ -760,35 +766,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < QW; ++j)
 #pragma unroll
                     for (int k = 0; k < NACC; ++k) a4[j][k] = 0ull;
-                // relu(x) * w summed per query: 4 chunks of 32 columns, the load
-                // of the next chunk overlapping the math on the current one
+                // relu(x) * w summed per query over this warp's 128 columns: all four
+                // 32-column TMEM loads in flight at once, one wait
                 auto accum = [&](const uint32_t(&v)[32], const int c0) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 2) {
+                    for (int x = 0; x < 32; x += 4) {
                         const int col = c0 + x;
                         const int j = col / H;
-                        const int k = (col / 2) % NACC;
-                        const uint64_t r = ptx::pack_f32x2(fmaxf(__uint_as_float(v[x]), 0.f),
-                                                           fmaxf(__uint_as_float(v[x + 1]), 0.f));
-                        a4[j][k] = ptx::ffma2(r, w2[col / 2], a4[j][k]);
+                        const int k = (col / 4) % NACC;
+                        const ulonglong2 wv = w4[col / 4];
+                        const uint64_t r0 = ptx::pack_f32x2(fmaxf(__uint_as_float(v[x]), 0.f),
+                                                            fmaxf(__uint_as_float(v[x + 1]), 0.f));
+                        const uint64_t r1 = ptx::pack_f32x2(fmaxf(__uint_as_float(v[x + 2]), 0.f),
+                                                            fmaxf(__uint_as_float(v[x + 3]), 0.f));
+                        a4[j][k] = ptx::ffma2(r0, wv.x, a4[j][k]);
+                        a4[j][k] = ptx::ffma2(r1, wv.y, a4[j][k]);
                     }
                 };
-                uint32_t va[32], vb[32];
-                ptx::tmem_ld32(tb, va);
-                ptx::tmem_ld_wait(va);
-                ptx::tmem_ld32(tb + 32, vb);
-                accum(va, 0);
-                ptx::tmem_ld_wait(vb);
-                ptx::tmem_ld32(tb + 64, va);
-                accum(vb, 32);
-                ptx::tmem_ld_wait(va);
-                ptx::tmem_ld32(tb + 96, vb);
-                accum(va, 64);
-                ptx::tmem_ld_wait(vb);
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                ptx::tmem_ld32(tb, v0);
+                ptx::tmem_ld32(tb + 32, v1);
+                ptx::tmem_ld32(tb + 64, v2);
+                ptx::tmem_ld32(tb + 96, v3);
+                ptx::tmem_ld_wait4(v0, v1, v2, v3);
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
-                accum(vb, 96);
+                accum(v0, 0);
+                accum(v1, 32);
+                accum(v2, 64);
+                accum(v3, 96);
                 if (++acc == 2) { acc = 0; acc_ph ^= 1; }
 
                 const int pool_local = i * kBM + qr * 32 + lane;
