@@ -135,6 +135,22 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def job_time_ms(local_ms, world, device=None):
+    """Whole-job step time: the max of the per-rank times over all ranks."""
+    if world <= 1:
+        return float(local_ms)
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units processed by all ranks per second (weak scaling: each rank runs
+    its own replica of the workload)."""
+    return world * units_per_rank / (ms / 1000.0)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -343,10 +359,7 @@ def main():
     t_compress = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     t_score = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     t_expand = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = job_time_ms(ms_step, world, dev)
     status = K.kpool_read_status(ws)
     if status != 0:
         raise RuntimeError("device status %d after the timed steps" % status)
@@ -381,11 +394,8 @@ def main():
         torch.cuda.synchronize()
         barrier()
         ms_e2e = a0.elapsed_time(a1) / n_e2e
-        if world > 1:
-            tt = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
-        e2e = {"value": world * T / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
+        ms_e2e = job_time_ms(ms_e2e, world, dev)
+        e2e = {"value": whole_job_rate(T, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
                "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del dq, dk, dg, da, dw, hq
 
@@ -425,7 +435,7 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": world * T / (ms_step / 1000.0), "unit": UNIT,
+            "metric": METRIC, "value": whole_job_rate(T, world, ms_step), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp8-e4m3" if wl.fp8 else "bf16", "data": "synthetic",

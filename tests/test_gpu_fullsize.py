@@ -1,0 +1,117 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times (persistent grid over all SMs), on sampled query rows the
+oracle computes one by one: 1024 seeded rows plus the first and last 64
+(per sequence for the FP8 batch).
+
+* long_128k: T = 131072, H = 64, D = 128, kpool = 4, index_topk = 2048.
+  The scorer is checked on the oracle's pooled keys (scores within
+  1e-3 * S, selections equal up to near-tie swaps); the whole path
+  (compress -> score/top-k -> expand) is checked for pooled keys, for the
+  structure of every row, and bit-exact expansion of the sampled rows.
+* fp8_2x32k: two sequences of 32768 tokens, E4M3 scoring.  End to end
+  against the oracle's own FP8 chain with the FP8 tolerance 5e-2 * S.
+"""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_kpool_compress_gb300 import workloads as W
+from kpool_checks import bf16_bits, check_pooled_keys, check_selection
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOL = 1e-3
+TOL_FP8 = 5e-2
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_attention_kpool_compress_gb300 as K
+    return K
+
+
+def _bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def _row_structure(idx, T, kp, Kp, cu):
+    """Every row: the first min(n_c, Kp) entries valid, strictly ascending,
+    inside the row's complete causal pools; the rest -1."""
+    cu = np.asarray(cu, np.int64)
+    cp = np.concatenate([[0], np.cumsum((cu[1:] - cu[:-1]) // kp)])
+    t = np.arange(T)
+    d = np.searchsorted(cu, t, side="right") - 1
+    tau = t - cu[d]
+    nsel = np.minimum((tau + 1) // kp, Kp)
+    col = np.arange(Kp)[None, :]
+    valid = col < nsel[:, None]
+    assert np.all((idx >= 0) == valid)
+    lo = cp[d][:, None]
+    hi = (cp[d] + (tau + 1) // kp)[:, None]
+    assert np.all(~valid | ((idx >= lo) & (idx < hi)))
+    diffs = np.diff(idx, axis=1)
+    assert np.all(~valid[:, 1:] | (diffs > 0))
+
+
+def test_long_128k(K, ora):
+    wl = W.WORKLOADS["long_128k"]
+    inp = W.make_inputs(wl)
+    T, kp, Kp = wl.T, wl.kpool, wl.Kp
+    dev = torch.device("cuda")
+    q, k, gate, ape, w = (x.to(dev) for x in (inp.q, inp.k, inp.gate, inp.ape, inp.w))
+    ws = K.new_workspace(T, wl.H, 1, dev)
+    # the whole path on the GPU
+    tok, idx, sc = K.kpool_indexer_forward(q, k, gate, ape, w, kp, wl.index_topk, True,
+                                           workspace=ws)
+    pk_gpu = K.kpool_compress(k, gate, ape, kp)
+    # the scorer alone on the oracle's pooled keys
+    pkb, exact, cond = ora.compress(W.bits(inp.k), W.bits(inp.gate), inp.ape.numpy(), None, kp,
+                                    want_cond=True)
+    idx_o, sc_o = K.kpool_score_topk(q, w, _bf16(pkb).to(dev), kp, wl.index_topk, workspace=ws)
+    torch.cuda.synchronize()
+    assert K.kpool_read_status(ws) == 0
+    check_pooled_keys(bf16_bits(pk_gpu), pkb, exact, cond, "long_128k")
+    rows = W.sample_rows(T).numpy()
+    ops = ora.Operands(W.bits(inp.q), inp.w.numpy(), pkb)
+    st = check_selection(ora, ops, None, kp, Kp, rows, idx_o.cpu().numpy()[rows],
+                         sc_o.cpu().numpy()[rows], TOL, "long_128k")
+    assert st["swaps"] <= 4
+    idx_h = idx.cpu().numpy()
+    _row_structure(idx_h, T, kp, Kp, [0, T])
+    want = ora.expand_rows(idx_h[rows], None, T, kp, Kp, True, rows)
+    assert np.array_equal(tok.cpu().numpy()[rows], want)
+
+
+def test_fp8_2x32k(K, ora):
+    wl = W.WORKLOADS["fp8_2x32k"]
+    inp = W.make_inputs(wl)
+    T, kp, Kp, H = wl.T, wl.kpool, wl.Kp, wl.H
+    cu = inp.cu_seqlens
+    cu_pools, P = K.kpool_num_pools(cu, T, kp)
+    dev = torch.device("cuda")
+    q, k, gate, ape, w = (x.to(dev) for x in (inp.q, inp.k, inp.gate, inp.ape, inp.w))
+    cud, cpd = cu.to(dev), cu_pools.to(dev)
+    tok, idx, sc = K.kpool_indexer_forward(q, k, gate, ape, w, kp, wl.index_topk, True, cud, cpd,
+                                           P, fp8=True)
+    torch.cuda.synchronize()
+    idx_h = idx.cpu().numpy()
+    _row_structure(idx_h, T, kp, Kp, cu.numpy())
+    # oracle FP8 chain: its own pooled keys, Hadamard, BF16, E4M3 and scales
+    pkb = ora.compress(W.bits(inp.k), W.bits(inp.gate), inp.ape.numpy(), cu.numpy(), kp)
+    pc, ps = ora.fp8_rows(pkb)
+    L = T // 2
+    rows = np.concatenate([W.sample_rows(T, lo=0, hi=L).numpy(),
+                           W.sample_rows(T, lo=L, hi=T, seed=1).numpy()])
+    qc = np.zeros((T, H, 128), np.uint8)
+    qs = np.ones((T, H), np.float32)
+    rc, rs = ora.fp8_rows(W.bits(inp.q)[rows].reshape(-1, 128))
+    qc[rows] = rc.reshape(len(rows), H, 128)
+    qs[rows] = rs.reshape(len(rows), H)
+    ops = ora.Operands(qc, inp.w.numpy(), pc, qs, ps)
+    st = check_selection(ora, ops, cu.numpy(), kp, Kp, rows, idx_h[rows], sc.cpu().numpy()[rows],
+                         TOL_FP8, "fp8_2x32k")
+    assert st["swaps"] <= len(rows)
+    want = ora.expand_rows(idx_h[rows], cu.numpy(), T, kp, Kp, True, rows)
+    assert np.array_equal(tok.cpu().numpy()[rows], want)
