@@ -108,12 +108,17 @@ __device__ __forceinline__ void fp8_row(float (&x)[8], int v, uint8_t *codes8, f
     if (v == 0) *scale_out = s;
 }
 
+// KP > 0: kpool known at compile time -- every slot's 16-byte gate and key
+// vectors are loaded up front and the softmax weights stay in registers.
+// KP == 0: any kpool, slots re-read from L1 in three passes.
+template <int KP>
 __global__ void __launch_bounds__(kThreads) compress_kernel(
     const uint16_t *__restrict__ k, const uint16_t *__restrict__ gate,
     const float *__restrict__ ape, const int32_t *__restrict__ cu_seqlens,
-    const int32_t *__restrict__ cu_pools, int n_docs, int D, int kp, int64_t P_total,
+    const int32_t *__restrict__ cu_pools, int n_docs, int D, int kp_rt, int64_t P_total,
     uint16_t *__restrict__ pk, uint8_t *__restrict__ pk_fp8, float *__restrict__ pk_scale)
 {
+    const int kp = KP > 0 ? KP : kp_rt;
     const int vpr = D >> 3;
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t g = gid / vpr;
@@ -133,6 +138,44 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(
             tok0 = g * kp;
         }
         const int col = v * 8;
+        if constexpr (KP > 0) {
+            uint4 gq[KP], kq[KP];
+#pragma unroll
+            for (int s = 0; s < KP; ++s) {
+                gq[s] = __ldg(reinterpret_cast<const uint4 *>(gate + (tok0 + s) * D + col));
+                kq[s] = __ldg(reinterpret_cast<const uint4 *>(k + (tok0 + s) * D + col));
+            }
+            float a[KP][8], m[8], z[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; z[i] = 0.f; }
+#pragma unroll
+            for (int s = 0; s < KP; ++s) {
+                float gv[8];
+                bf16x8_to_f32(gq[s], gv);
+                const float4 a0 = __ldg(reinterpret_cast<const float4 *>(ape + s * D + col));
+                const float4 a1 = __ldg(reinterpret_cast<const float4 *>(ape + s * D + col + 4));
+                const float ap[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    a[s][i] = gv[i] + ap[i];
+                    m[i] = fmaxf(m[i], a[s][i]);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < KP; ++s)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    a[s][i] = expf(a[s][i] - m[i]);
+                    z[i] += a[s][i];
+                }
+#pragma unroll
+            for (int s = 0; s < KP; ++s) {
+                float kv[8];
+                bf16x8_to_f32(kq[s], kv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(__fdiv_rn(a[s][i], z[i]), kv[i], acc[i]);
+            }
+        } else {
         float m[8], z[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; z[i] = 0.f; }
@@ -167,6 +210,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(
                 const float alpha = __fdiv_rn(expf((gv[i] + ap[i]) - m[i]), z[i]);
                 acc[i] = fmaf(alpha, kv[i], acc[i]);
             }
+        }
         }
         uint32_t o[4];
 #pragma unroll
@@ -231,9 +275,18 @@ cudaError_t launch_compress(const void *k, const void *gate, const float *ape,
     if (P_total == 0) return cudaSuccess;
     const int64_t threads = P_total * (D / 8);
     const int64_t blocks = (threads + kThreads - 1) / kThreads;
-    compress_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
-        static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(gate), ape, cu_seqlens,
-        cu_pools, n_docs, D, kpool, P_total, static_cast<uint16_t *>(pk_out), pk_fp8, pk_scale);
+#define KPOOL_COMPRESS_LAUNCH(KP)                                                              \
+    compress_kernel<KP><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(                     \
+        static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(gate), ape, cu_seqlens, \
+        cu_pools, n_docs, D, kpool, P_total, static_cast<uint16_t *>(pk_out), pk_fp8, pk_scale)
+    switch (kpool) {
+    case 1: KPOOL_COMPRESS_LAUNCH(1); break;
+    case 2: KPOOL_COMPRESS_LAUNCH(2); break;
+    case 4: KPOOL_COMPRESS_LAUNCH(4); break;
+    case 8: KPOOL_COMPRESS_LAUNCH(8); break;
+    default: KPOOL_COMPRESS_LAUNCH(0); break;
+    }
+#undef KPOOL_COMPRESS_LAUNCH
     return cudaGetLastError();
 }
 

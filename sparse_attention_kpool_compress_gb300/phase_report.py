@@ -1,0 +1,75 @@
+"""Per-phase cycle breakdown of the scoring kernel (diagnostics).
+
+Builds the ``phase_timers`` variant of the library (``-DKPOOL_PHASE_TIMERS``:
+the same kernels plus clock64 counters around each wait and work phase),
+runs ``kpool_score_topk`` on random bf16 inputs of the requested size and
+prints, per role (epilogue warps, MMA thread, TMA producer thread), the share
+of cycles in each phase, summed over all CTAs.
+
+    python -m sparse_attention_kpool_compress_gb300.phase_report [T ...]
+"""
+from __future__ import annotations
+
+import ctypes
+import json
+import sys
+
+import torch
+
+from . import build as B
+
+EPI = ["wait_tile", "loop_overhead", "wait_tmem_full", "tmem_ld_and_math", "append",
+       "capacity_check_and_compaction", "final_select_and_store", "other"]
+MMA = ["wait_tile", "wait_q_full", "wait_tmem_empty", "wait_pk_full", "issue", "other"]
+PROD = ["wait_tile_slot", "wait_q_empty", "wait_pk_empty", "issue", "other"]
+
+
+def run(T: int, H: int = 64, D: int = 128, kpool: int = 4, index_topk: int = 2048, seed: int = 0):
+    lib = ctypes.CDLL(B.build(variant="phase_timers"))
+    P = ctypes.c_void_p
+    lib.kpool_score_topk_workspace_size.restype = ctypes.c_size_t
+    lib.kpool_score_topk_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    lib.kpool_score_topk.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_size_t, P]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    q = torch.randn(T, H, D, device="cuda", generator=g).to(torch.bfloat16)
+    pk = torch.randn(T // kpool, D, device="cuda", generator=g).to(torch.bfloat16)
+    w = torch.randn(T, H, device="cuda", generator=g) / H ** 0.5
+    Kp = index_topk // kpool
+    idx = torch.empty(T, Kp, dtype=torch.int32, device="cuda")
+    sc = torch.empty(T, Kp, dtype=torch.float32, device="cuda")
+    nws = lib.kpool_score_topk_workspace_size(T, H, 1)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+
+    def call():
+        rc = lib.kpool_score_topk(ptr(q), None, ptr(w), ptr(pk), None, None, None, 1, T,
+                                  T // kpool, H, D, kpool, index_topk, 0, ptr(idx), ptr(sc),
+                                  ptr(ws), nws, None)
+        if rc != 0:
+            raise RuntimeError(lib.kpool_last_error())
+
+    out = (ctypes.c_ulonglong * 32)()
+    call()
+    torch.cuda.synchronize()
+    lib.kpool_debug_phase_timers(out, 1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    call()
+    e1.record()
+    torch.cuda.synchronize()
+    lib.kpool_debug_phase_timers(out, 1)
+    v = list(out)
+    res = {"T": T, "H": H, "D": D, "kpool": kpool, "index_topk": index_topk,
+           "ms": e0.elapsed_time(e1)}
+    for key, base, names in (("epilogue", 24, EPI), ("mma", 8, MMA), ("producer", 16, PROD)):
+        tot = sum(v[base:base + 8]) or 1
+        res[key] = {n: round(100.0 * v[base + i] / tot, 1) for i, n in enumerate(names)}
+    return res
+
+
+if __name__ == "__main__":
+    for arg in sys.argv[1:] or ["131072"]:
+        print(json.dumps(run(int(arg))))
