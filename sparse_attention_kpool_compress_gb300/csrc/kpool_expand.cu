@@ -25,14 +25,18 @@ __device__ __forceinline__ int doc_of_token(const int32_t *cu, int n_docs, int64
     return lo;
 }
 
+constexpr int kStageInts = 512;   // per-warp staging of a row's pool list (larger Kp read directly)
+
 template <int KP>   // KP > 0: compile-time kpool; 0: runtime kp
 __global__ void __launch_bounds__(kThreads) expand_kernel(
     const int32_t *__restrict__ pool_idx, const int32_t *__restrict__ cu_seqlens,
     const int32_t *__restrict__ cu_pools, int n_docs, int64_t T, int kp_rt, int Kp, int tail,
     int32_t *__restrict__ out)
 {
+    __shared__ int32_t stage[kRowsPerBlock][kStageInts];
     const int kp = KP > 0 ? KP : kp_rt;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
+    const int wib = threadIdx.x >> 5;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + wib;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
     int64_t doc_start = 0, pool_lo = 0, pool_hi = T / kp;
@@ -50,18 +54,25 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(
     const int W = Kp * kp + kp - 1;
     const int32_t *row_in = pool_idx + t * Kp;
     int32_t *row_out = out + t * W;
+    // the row's selected pools, staged with coalesced loads
+    const bool staged = n_sel <= kStageInts;
+    int32_t *st = stage[wib];
+    if (staged) {
+        for (int e = lane; e < n_sel; e += 32) st[e] = __ldg(row_in + e);
+        __syncwarp();
+    }
     for (int c = lane; c < W; c += 32) {
         int32_t v = -1;
         if (c < n_pool_tok) {
             const int e = c / kp;
             const int s = c - e * kp;
-            const int32_t g = row_in[e];
+            const int32_t g = staged ? st[e] : row_in[e];
             if (g >= pool_lo && g < pool_hi)
                 v = static_cast<int32_t>(doc_start + (g - pool_lo) * kp + s);
         } else if (c < n_pool_tok + n_tail) {
             v = static_cast<int32_t>(t - n_tail + 1 + (c - n_pool_tok));
         }
-        row_out[c] = v;
+        __stcs(row_out + c, v);   // streaming store: the table is not re-read here
     }
 }
 
