@@ -89,18 +89,23 @@ __device__ __forceinline__ void fp8_row(float (&x)[8], int v, uint8_t *codes8, f
     for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
     // smallest power of two s with amax <= 448 s: amax = f * 2^E, f in [0.5, 1),
     // 448 = 0.875 * 2^9  ->  s = 2^(E - 9 + (f > 0.875)).
-    float s = 1.f;
+    int e = 0;
     if (amax > 0.f) {
         int E;
-        float f = frexpf(amax, &E);
-        s = ldexpf(1.f, E - 9 + (f > 0.875f ? 1 : 0));
+        const float f = frexpf(amax, &E);
+        e = E - 9 + (f > 0.875f ? 1 : 0);
     }
+    const float s = ldexpf(1.f, e);
     if (!active) return;
+    // x / s exactly: a multiply by the power of two 2^-e when that is a normal
+    // float, otherwise an exact exponent shift
+    const bool mul_ok = e > -126 && e < 126;
+    const float inv = mul_ok ? ldexpf(1.f, -e) : 1.f;
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        uint32_t c = static_cast<uint32_t>(
-            __nv_cvt_float_to_fp8(__fdiv_rn(x[i], s), __NV_SATFINITE, __NV_E4M3));
+        const float y = mul_ok ? x[i] * inv : ldexpf(x[i], -e);
+        uint32_t c = static_cast<uint32_t>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
         if (i < 4) lo |= c << (8 * i);
         else hi |= c << (8 * (i - 4));
     }

@@ -35,9 +35,9 @@
 namespace kpool {
 namespace {
 
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = 32 * kEpiWarps;           // 256
-constexpr int kThreads = 128 + kEpiThreads;           // 384
+constexpr int kEpiWarps = 16;                         // 4 per SM sub-partition
+constexpr int kEpiThreads = 32 * kEpiWarps;           // 512
+constexpr int kThreads = 128 + kEpiThreads;           // 640
 constexpr int kBM = 128;                              // pools per tile
 constexpr int kBN = 256;                              // (query, head) columns per tile
 constexpr int kAccCols = 256;
@@ -47,11 +47,11 @@ constexpr int kMaxC = 4096;
 constexpr uint64_t kTimeoutNs = 2000000000ull;        // 2 s per wait
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kGroups = 4;                            // selection groups of the epilogue
-constexpr int kGroupWarps = kEpiWarps / kGroups;      // 2 warps per group
-constexpr int kGroupThreads = 32 * kGroupWarps;       // 64
+constexpr int kGroupWarps = kEpiWarps / kGroups;      // 4 warps per group
+constexpr int kGroupThreads = 32 * kGroupWarps;       // 128
 constexpr int kSlack = 64;                            // extra entries a mid-stream prune may keep
-// register split (setmaxnreg): 128 threads x 56 + 256 x 224 = 384 x 168
-constexpr int kRegsOther = 56, kRegsEpi = 224;
+// register split (setmaxnreg): 128 threads x 32 + 512 x 112 = 640 x 96 (launch budget)
+constexpr int kRegsOther = 32, kRegsEpi = 112;
 
 // Optional phase timers (build with -DKPOOL_PHASE_TIMERS): per-role cycle
 // counts of waits and work, summed over all CTAs into g_phase_timers and read
@@ -110,7 +110,7 @@ Layout make_layout(int H, int D, int fp8)
     L.pk_off = L.q_off + L.n_kchunks * L.q_chunk;
     L.pk_stage = L.n_kchunks * L.pk_chunk;
     uint32_t off = L.pk_off + L.stages * L.pk_stage;
-    L.ws_off = off;   off += kEpiWarps * 128 * 4;   // head weights of each epilogue warp
+    L.ws_off = off;   off += (kBN + 2 * 4 * kBM) * 4;   // head weights + half-query partials
     L.hist_off = off; off += kGroups * 256 * 4;
     L.cnt_off = off;  off += 2 * QT * 4 * 4;
     L.scr_off = off;  off += kGroups * 32 * 4 + ((QT * 4 + 15) / 16) * 16;
@@ -225,13 +225,19 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
     cnt = __reduce_add_sync(kFull, cnt);
     if (lane == 0) {
         gs[gw] = static_cast<int>(kmin);
-        gs[2 + gw] = static_cast<int>(kmax);
-        gs[4 + gw] = cnt;
+        gs[4 + gw] = static_cast<int>(kmax);
+        gs[8 + gw] = cnt;
     }
     group_bar(g);
-    kmin = min(static_cast<uint32_t>(gs[0]), static_cast<uint32_t>(gs[1]));
-    kmax = max(static_cast<uint32_t>(gs[2]), static_cast<uint32_t>(gs[3]));
-    cnt = gs[4] + gs[5];
+    kmin = 0xFFFFFFFFu;
+    kmax = 0u;
+    cnt = 0;
+#pragma unroll
+    for (int w = 0; w < kGroupWarps; ++w) {
+        kmin = min(kmin, static_cast<uint32_t>(gs[w]));
+        kmax = max(kmax, static_cast<uint32_t>(gs[4 + w]));
+        cnt += gs[8 + w];
+    }
     above = 0;
     if (kmin == kmax) {
         kth = kmax;
@@ -272,15 +278,15 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
 #pragma unroll
             for (int i = 7; i >= 0; --i) {
                 if (cum < kr && cum + b[i] >= kr) {
-                    gs[8] = lane * 8 + i;
-                    gs[9] = cum;
-                    gs[10] = b[i];
+                    gs[12] = lane * 8 + i;
+                    gs[13] = cum;
+                    gs[14] = b[i];
                 }
                 cum += b[i];
             }
         }
         group_bar(g);
-        const int d = gs[8], cum = gs[9], hb = gs[10];
+        const int d = gs[12], cum = gs[13], hb = gs[14];
         prefix |= static_cast<uint32_t>(d) << lo;
         kr -= cum;
         above += cum;
@@ -686,10 +692,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         ptx::setmaxnreg_inc<kRegsEpi>();
         // ---------------- epilogue ----------------
-        constexpr int NACC = H >= 32 ? 4 : (H >= 16 ? 2 : 1);   // FFMA2 chains per query
+        // 16 warps: warp (slice, quarter) reads TMEM lanes 32*quarter.. (its 32
+        // pools) and columns 64*slice.. of the 256 (query, head) columns.
+        constexpr int SLICE = 64;                                  // columns per warp
+        constexpr bool kHalfQ = H > SLICE;                         // a query spans two slices
+        constexpr int QS = kHalfQ ? 1 : SLICE / H;                 // queries per warp
+        constexpr int NACC = H >= 32 ? 4 : (H >= 16 ? 2 : 1);     // FFMA2 chains per query
         const int ew = warp - 4;
         const int qr = warp & 3;            // TMEM lane quarter
-        const int hf = ew >> 2;             // which half of the 256 columns
+        const int sl = ew >> 2;             // column slice
+        const int qbase = kHalfQ ? (sl >> 1) : sl * QS;   // first query of this warp
+        const bool owner = !kHalfQ || (sl & 1) == 0;      // appends the query's score
         const int etid = threadIdx.x - 128;
         const int g = ew / kGroupWarps;     // selection group
         const int gtid = etid - g * kGroupThreads;
@@ -699,6 +712,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t *thr_s = reinterpret_cast<uint32_t *>(smem + L.thr_off);
         float *cs = reinterpret_cast<float *>(smem + L.cs_off);
         int *ci = reinterpret_cast<int *>(smem + L.ci_off);
+        float *wsm = reinterpret_cast<float *>(smem + L.ws_off);  // 256 head weights
+        float *part = wsm + kBN;                                   // [2][4][128] partial scores
+        const ulonglong2 *w4 = reinterpret_cast<const ulonglong2 *>(wsm + sl * SLICE);
         const int C = L.C;
         const int Kp = p.Kp;
         const int slack = max(0, min(kSlack, C - kBM - Kp));
@@ -707,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int G = max(1, min(4, (C - Kp - slack) / kBM));
         const int room = C - G * kBM;
         const unsigned lt = (1u << lane) - 1u;
-        int acc = 0;
+        int acc = 0, tile_seq = 0;
         uint32_t acc_ph = 0;
         PT_DECL
         for (int it = 0;; ++it) {
@@ -724,33 +740,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nq = min(QT, t.doc_end - t.t0);
             const int npt = pool_tiles_of(t, QT, p.kp);
 
-            // this warp's 128 head weights (w, times q_scale in FP8 mode), staged in
+            // the tile's 256 head weights (w, times q_scale in FP8 mode), staged in
             // shared memory once per query tile and read back as broadcasts
-            float *wsm = reinterpret_cast<float *>(smem + L.ws_off) + ew * 128;
-            __syncwarp();
-            {
-                const int c = lane * 4;
-                const int qi = hf * QW + c / H;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (etid < kBN) {
+                const int qi = etid / H;
+                float v = 0.f;
                 if (qi < nq) {
-                    const int64_t off = static_cast<int64_t>(t.t0 + hf * QW) * H + c;
-                    v = __ldg(reinterpret_cast<const float4 *>(p.w + off));
-                    if (p.fp8) {
-                        const float4 s4 = __ldg(reinterpret_cast<const float4 *>(p.q_scale + off));
-                        v.x *= s4.x; v.y *= s4.y; v.z *= s4.z; v.w *= s4.w;
-                    }
+                    const int64_t off = static_cast<int64_t>(t.t0) * H + etid;
+                    v = __ldg(p.w + off);
+                    if (p.fp8) v *= __ldg(p.q_scale + off);
                 }
-                *reinterpret_cast<float4 *>(wsm + c) = v;
+                wsm[etid] = v;
             }
-            __syncwarp();
-            const ulonglong2 *w4 = reinterpret_cast<const ulonglong2 *>(wsm);
+            ptx::named_bar_sync(1, kEpiThreads);
 
-            uint32_t thr[QW];
-            int nc[QW];
+            uint32_t thr[QS];
+            int nc[QS];
 #pragma unroll
-            for (int j = 0; j < QW; ++j) {
+            for (int j = 0; j < QS; ++j) {
                 thr[j] = 0u;
-                nc[j] = (tau0 + hf * QW + j + 1) / p.kp;
+                nc[j] = (tau0 + qbase + j + 1) / p.kp;
             }
             bool aborted = false;
 
@@ -760,19 +769,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 PT_MARK(2);
                 ptx::tc_fence_after();
                 const uint32_t tb = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) +
-                                    acc * kAccCols + hf * 128;
-                uint64_t a4[QW][NACC];
+                                    acc * kAccCols + sl * SLICE;
+                uint32_t v0[32], v1[32];
+                ptx::tmem_ld32(tb, v0);
+                ptx::tmem_ld32(tb + 32, v1);
+                ptx::tmem_ld_wait2(v0, v1);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
+                if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+
+                // relu(x) * w summed per query over this warp's 64 columns
+                uint64_t a4[QS][NACC];
 #pragma unroll
-                for (int j = 0; j < QW; ++j)
+                for (int j = 0; j < QS; ++j)
 #pragma unroll
                     for (int k = 0; k < NACC; ++k) a4[j][k] = 0ull;
-                // relu(x) * w summed per query over this warp's 128 columns: all four
-                // 32-column TMEM loads in flight at once, one wait
                 auto accum = [&](const uint32_t(&v)[32], const int c0) {
 #pragma unroll
                     for (int x = 0; x < 32; x += 4) {
                         const int col = c0 + x;
-                        const int j = col / H;
+                        const int j = kHalfQ ? 0 : col / H;
                         const int k = (col / 4) % NACC;
                         const ulonglong2 wv = w4[col / 4];
                         const uint64_t r0 = ptx::pack_f32x2(fmaxf(__uint_as_float(v[x]), 0.f),
@@ -783,61 +800,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a4[j][k] = ptx::ffma2(r1, wv.y, a4[j][k]);
                     }
                 };
-                uint32_t v0[32], v1[32], v2[32], v3[32];
-                ptx::tmem_ld32(tb, v0);
-                ptx::tmem_ld32(tb + 32, v1);
-                ptx::tmem_ld32(tb + 64, v2);
-                ptx::tmem_ld32(tb + 96, v3);
-                ptx::tmem_ld_wait4(v0, v1, v2, v3);
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
                 accum(v0, 0);
                 accum(v1, 32);
-                accum(v2, 64);
-                accum(v3, 96);
-                if (++acc == 2) { acc = 0; acc_ph ^= 1; }
 
                 const int pool_local = i * kBM + qr * 32 + lane;
                 const int pool_g = t.pool_base + pool_local;
-                float sk = 1.f;
-                if (p.fp8 && pool_g < p.P_total) sk = p.pk_scale[pool_g];
-                float s[QW];
+                float s[QS];
 #pragma unroll
-                for (int j = 0; j < QW; ++j) {
+                for (int j = 0; j < QS; ++j) {
                     float v = ptx::sum_f32x2(a4[j][0]);
 #pragma unroll
                     for (int k = 1; k < NACC; ++k) v += ptx::sum_f32x2(a4[j][k]);
+                    s[j] = v;
+                }
+                if (kHalfQ) {
+                    // the two 64-head halves of a query meet in shared memory
+                    float *pt = part + (tile_seq & 1) * (4 * kBM);
+                    pt[sl * kBM + qr * 32 + lane] = s[0];
+                    ptx::named_bar_sync(1, kEpiThreads);
+                    if (owner) s[0] += pt[(sl + 1) * kBM + qr * 32 + lane];
+                }
+                ++tile_seq;
+                float sk = 1.f;
+                if (p.fp8 && pool_g < p.P_total) sk = p.pk_scale[pool_g];
+#pragma unroll
+                for (int j = 0; j < QS; ++j) {
+                    float v = s[j];
                     if (p.fp8) v *= sk;
                     s[j] = (v == 0.f) ? 0.f : v;   // fold -0 into +0
                 }
                 PT_MARK(3);
 
                 if (p.mode == 1) {   // dense scores (test/debug)
+                    if (owner) {
 #pragma unroll
-                    for (int j = 0; j < QW; ++j) {
-                        const int qi = hf * QW + j;
-                        if (qi < nq && pool_local < nc[j])
-                            p.scores[static_cast<int64_t>(t.t0 + qi) * p.P_total + pool_g] = s[j];
+                        for (int j = 0; j < QS; ++j) {
+                            const int qi = qbase + j;
+                            if (qi < nq && pool_local < nc[j])
+                                p.scores[static_cast<int64_t>(t.t0 + qi) * p.P_total + pool_g] =
+                                    s[j];
+                        }
                     }
                     continue;
                 }
 
                 // survivors of the threshold filter, appended (unordered) with one
                 // shared-memory atomic per warp and query that has any
+                if (owner) {
 #pragma unroll
-                for (int j = 0; j < QW; ++j) {
-                    const int qi = hf * QW + j;
-                    const bool ps = (qi < nq) && (pool_local < nc[j]) && (fkey(s[j]) > thr[j]);
-                    const unsigned bal = __ballot_sync(kFull, ps);
-                    if (bal != 0u) {
-                        int base = 0;
-                        if (lane == 0) base = atomicAdd(&qcnt[qi], __popc(bal));
-                        base = __shfl_sync(kFull, base, 0);
-                        if (ps) {
-                            const int d = qi * C + base + __popc(bal & lt);
-                            cs[d] = s[j];
-                            ci[d] = pool_g;
+                    for (int j = 0; j < QS; ++j) {
+                        const int qi = qbase + j;
+                        const bool ps = (qi < nq) && (pool_local < nc[j]) && (fkey(s[j]) > thr[j]);
+                        const unsigned bal = __ballot_sync(kFull, ps);
+                        if (bal != 0u) {
+                            int base = 0;
+                            if (lane == 0) base = atomicAdd(&qcnt[qi], __popc(bal));
+                            base = __shfl_sync(kFull, base, 0);
+                            if (ps) {
+                                const int d = qi * C + base + __popc(bal & lt);
+                                cs[d] = s[j];
+                                ci[d] = pool_g;
+                            }
                         }
                     }
                 }
@@ -859,13 +882,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ptx::named_bar_sync(1, kEpiThreads);
 #pragma unroll
-                        for (int j = 0; j < QW; ++j) thr[j] = thr_s[hf * QW + j];
+                        for (int j = 0; j < QS; ++j) thr[j] = thr_s[qbase + j];
                     }
                     PT_MARK(5);
                 }
             }
             if (aborted) break;
-            if (p.mode == 1) continue;
+            if (p.mode == 1) {
+                ptx::named_bar_sync(1, kEpiThreads);   // w staging is rewritten next
+                continue;
+            }
 
             // final selection, pool order and output: every group on its own queries
             PT_MARK(1);
