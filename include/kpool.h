@@ -176,6 +176,41 @@ KPOOL_API int kpool_score_topk(const void *q, const float *q_scale, const float 
                      void *workspace, size_t workspace_bytes, kpool_stream_t stream);
 
 /*
+ * kpool_score_topk_at -- kpool_score_topk for query rows at given positions
+ * of their documents (decode and chunked prefill: the queries are fewer than
+ * the keys).  Document d's query rows are [cu_seqlens_q[d], cu_seqlens_q[d+1])
+ * of q and w; its i-th query row sits at document-local position
+ * q_start_pos[d] + i of the key sequence whose pooled keys are
+ * pk[cu_pools[d] .. cu_pools[d+1]) (from kpool_compress on the keys).  A query
+ * at position tau scores the complete pools j < floor((tau+1)/kpool), clamped
+ * to the document's pools.  With q_start_pos = 0 and the keys' cu_seqlens as
+ * cu_seqlens_q this is kpool_score_topk.  All three index arrays are device
+ * int32 and required; Tq = cu_seqlens_q[n_docs]; the workspace is sized by
+ * kpool_score_topk_workspace_size(Tq, H, n_docs).  Outputs as in
+ * kpool_score_topk (global pool indices, ascending).
+ */
+KPOOL_API int kpool_score_topk_at(const void *q, const float *q_scale, const float *w,
+                                  const void *pk, const float *pk_scale,
+                                  const int32_t *cu_seqlens_q, const int32_t *q_start_pos,
+                                  const int32_t *cu_pools, int n_docs, int64_t Tq, int64_t P_total,
+                                  int H, int D, int kpool, int index_topk, int fp8,
+                                  int32_t *pool_idx_out, float *pool_score_out, void *workspace,
+                                  size_t workspace_bytes, kpool_stream_t stream);
+
+/*
+ * kpool_expand_indices_at -- kpool_expand_indices for positioned queries:
+ * pool p of document d expands to key tokens cu_seqlens_k[d] + j*kpool + s,
+ * and the tail of a query at position tau is the key tokens
+ * cu_seqlens_k[d] + tau - r + 1 .. cu_seqlens_k[d] + tau, r = (tau+1) mod
+ * kpool (the query's own token must lie in its key sequence).
+ */
+KPOOL_API int kpool_expand_indices_at(const int32_t *pool_idx, const int32_t *cu_seqlens_q,
+                                      const int32_t *q_start_pos, const int32_t *cu_seqlens_k,
+                                      const int32_t *cu_pools, int n_docs, int64_t Tq, int kpool,
+                                      int index_topk, int always_select_tail,
+                                      int32_t *tok_idx_out, kpool_stream_t stream);
+
+/*
  * kpool_score_topk_noalloc -- the same computation, arguments and outputs as
  * kpool_score_topk, for callers that cannot allocate device memory: code
  * running where cudaMalloc is not allowed or not wanted, such as inside a

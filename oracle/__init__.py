@@ -83,6 +83,11 @@ def _load():
             "ora_score_rows_full": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                            i64, P, i64, P, P]),
             "ora_expand_rows": (None, [P, P, i32, i32, i32, i32, P, i64, P]),
+            "ora_score_pairs_at": (None, [P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32, i64,
+                                          P, P, i64, P, P]),
+            "ora_select_rows_at": (None, [P, P, P, P, P, i32, P, P, P, i32, i32, i32, i32, i64,
+                                          i32, P, i64, P, P, P, P, P]),
+            "ora_expand_rows_at": (None, [P, P, P, P, i32, i32, i32, i32, P, i64, P]),
             "ora_num_threads": (i32, []),
         }
         for name, (res, args) in sig.items():
@@ -265,4 +270,48 @@ def expand_rows(sel, cu_seqlens, T: int, kp: int, Kp: int, tail: bool, rows):
     out = np.empty((n, W), dtype=np.int32)
     _load().ora_expand_rows(_ptr(sel), _ptr(cs), len(cs) - 1, kp, Kp, int(bool(tail)),
                             _ptr(rows), n, _ptr(out))
+    return out
+
+
+# -- queries at given positions (decode / chunked prefill) --------------------
+# Document d's query rows are [cu_q[d], cu_q[d+1]) of q (and w); its i-th query
+# sits at document-local position q_pos[d] + i of a key sequence whose tokens
+# are [cu_k[d], cu_k[d+1]) (pooled keys: floor(L_k / kpool) per document).
+
+def select_rows_at(ops: Operands, cu_q, q_pos, cu_k, kp: int, Kp: int, rows):
+    cq, qp, ck = _c(cu_q, np.int32), _c(q_pos, np.int32), _c(cu_k, np.int32)
+    rows = _c(rows, np.int64)
+    n = len(rows)
+    sel = np.empty((n, Kp), dtype=np.int32)
+    sel_score = np.empty((n, Kp), dtype=np.float64)
+    kth = np.empty(n, dtype=np.float64)
+    kth_cond = np.empty(n, dtype=np.float64)
+    n_sel = np.empty(n, dtype=np.int32)
+    _load().ora_select_rows_at(*ops.args(), _ptr(cq), _ptr(qp), _ptr(ck), len(cq) - 1, ops.H,
+                               ops.D, kp, ops.P, Kp, _ptr(rows), n, _ptr(sel), _ptr(sel_score),
+                               _ptr(kth), _ptr(kth_cond), _ptr(n_sel))
+    return dict(sel=sel, sel_score=sel_score, kth=kth, kth_cond=kth_cond, n_sel=n_sel)
+
+
+def score_pairs_at(ops: Operands, cu_q, q_pos, cu_k, kp: int, rows, pools):
+    cq, qp, ck = _c(cu_q, np.int32), _c(q_pos, np.int32), _c(cu_k, np.int32)
+    rows = _c(rows, np.int64)
+    pools = _c(pools, np.int64)
+    n = len(rows)
+    sc = np.empty(n, dtype=np.float64)
+    cd = np.empty(n, dtype=np.float64)
+    _load().ora_score_pairs_at(*ops.args(), _ptr(cq), _ptr(qp), _ptr(ck), len(cq) - 1, ops.H,
+                               ops.D, kp, ops.P, _ptr(rows), _ptr(pools), n, _ptr(sc), _ptr(cd))
+    return sc, cd
+
+
+def expand_rows_at(sel, cu_q, q_pos, cu_k, kp: int, Kp: int, tail: bool, rows):
+    cq, qp, ck = _c(cu_q, np.int32), _c(q_pos, np.int32), _c(cu_k, np.int32)
+    rows = _c(rows, np.int64)
+    sel = _c(sel, np.int32)
+    n = len(rows)
+    W = Kp * kp + kp - 1
+    out = np.empty((n, W), dtype=np.int32)
+    _load().ora_expand_rows_at(_ptr(sel), _ptr(cq), _ptr(qp), _ptr(ck), len(cq) - 1, kp, Kp,
+                               int(bool(tail)), _ptr(rows), n, _ptr(out))
     return out

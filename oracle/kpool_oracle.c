@@ -383,27 +383,53 @@ static void score_pair(const ora_operands *o, const double *qd, int64_t t, int64
 /* Number of complete causal pools for document-local position tau. */
 static int64_t n_complete(int64_t tau, int kp) { return (tau + 1) / kp; }
 
-/* Scores for an explicit list of (row, global pool) pairs.  A pair whose pool
- * is not a complete causal pool of the row's document gets -inf / 0. */
-void ora_score_pairs(const void *q, const float *qs, const float *w, const void *pk,
-                     const float *pks, int fp8, const int32_t *cu_seqlens, int n_docs,
-                     int H, int D, int kp, int64_t P, const int64_t *rows, const int64_t *pools,
-                     int64_t n_pairs, double *score_out, double *cond_out)
+/* Where query rows sit.  Document d's query rows are [cu_q[d], cu_q[d+1]); its
+ * i-th query row is at document-local position q_pos[d] + i (q_pos NULL: 0, the
+ * plain case where every key token is also a query).  Its keys are the tokens
+ * [cu_k[d], cu_k[d+1]) with floor(L_k / kp) complete pools.  A query sees the
+ * complete pools j < min(floor((tau+1)/kp), pools of its document). */
+typedef struct {
+    const int32_t *cu_q;
+    const int32_t *q_pos;
+    const int32_t *cu_k;
+    const int32_t *cu_pools;
+    int n_docs;
+} ora_layout;
+
+static int layout_row(const ora_layout *L, int64_t t, int64_t *tau, int64_t *nc, int kp)
+{
+    int d = doc_of_token(L->cu_q, L->n_docs, t);
+    if (d < 0) return -1;
+    *tau = (L->q_pos ? L->q_pos[d] : 0) + (t - L->cu_q[d]);
+    int64_t npool = (int64_t)L->cu_pools[d + 1] - L->cu_pools[d];
+    int64_t c = n_complete(*tau, kp);
+    *nc = c < npool ? c : npool;
+    return d;
+}
+
+/* Scores for an explicit list of (query row, global pool) pairs.  A pair
+ * whose pool is not a visible complete pool of the row's document gets
+ * -inf / 0. */
+void ora_score_pairs_at(const void *q, const float *qs, const float *w, const void *pk,
+                        const float *pks, int fp8, const int32_t *cu_q, const int32_t *q_pos,
+                        const int32_t *cu_k, int n_docs, int H, int D, int kp, int64_t P,
+                        const int64_t *rows, const int64_t *pools, int64_t n_pairs,
+                        double *score_out, double *cond_out)
 {
     ora_operands o;
     ops_init(&o, q, qs, w, pk, pks, fp8, H, D, P);
     int32_t *cu_pools = (int32_t *)malloc(sizeof(int32_t) * (n_docs + 1));
-    ora_cu_pools(cu_seqlens, n_docs, kp, cu_pools);
+    ora_cu_pools(cu_k, n_docs, kp, cu_pools);
+    ora_layout L = {cu_q, q_pos, cu_k, cu_pools, n_docs};
 #pragma omp parallel
     {
         double *qd = (double *)malloc(sizeof(double) * H * D);
 #pragma omp for schedule(dynamic, 16)
         for (int64_t i = 0; i < n_pairs; i++) {
-            int64_t t = rows[i], p = pools[i];
-            int doc = doc_of_token(cu_seqlens, n_docs, t);
-            int64_t tau = t - cu_seqlens[doc];
-            int64_t j = p - cu_pools[doc];
-            if (doc < 0 || j < 0 || j >= n_complete(tau, kp)) {
+            int64_t t = rows[i], p = pools[i], tau, nc;
+            int doc = layout_row(&L, t, &tau, &nc, kp);
+            int64_t j = doc < 0 ? -1 : p - cu_pools[doc];
+            if (doc < 0 || j < 0 || j >= nc) {
                 score_out[i] = -INFINITY;
                 cond_out[i] = 0.0;
                 continue;
@@ -415,6 +441,15 @@ void ora_score_pairs(const void *q, const float *qs, const float *w, const void 
     }
     free(cu_pools);
     ops_free(&o);
+}
+
+void ora_score_pairs(const void *q, const float *qs, const float *w, const void *pk,
+                     const float *pks, int fp8, const int32_t *cu_seqlens, int n_docs,
+                     int H, int D, int kp, int64_t P, const int64_t *rows, const int64_t *pools,
+                     int64_t n_pairs, double *score_out, double *cond_out)
+{
+    ora_score_pairs_at(q, qs, w, pk, pks, fp8, cu_seqlens, NULL, cu_seqlens, n_docs, H, D, kp, P,
+                       rows, pools, n_pairs, score_out, cond_out);
 }
 
 typedef struct {
@@ -444,25 +479,24 @@ static int i64_cmp(const void *a, const void *b)
  *   kth[r], kth_cond[r]  score and condition scale of the Kp-th best pool
  *                     (NaN / 0 when the row selects all of its pools)
  *   n_sel[r]          number of selected pools. */
-void ora_select_rows(const void *q, const float *qs, const float *w, const void *pk,
-                     const float *pks, int fp8, const int32_t *cu_seqlens, int n_docs,
-                     int H, int D, int kp, int64_t P, int Kp, const int64_t *rows, int64_t n_rows,
-                     int32_t *sel, double *sel_score, double *kth, double *kth_cond,
-                     int32_t *n_sel)
+void ora_select_rows_at(const void *q, const float *qs, const float *w, const void *pk,
+                        const float *pks, int fp8, const int32_t *cu_q, const int32_t *q_pos,
+                        const int32_t *cu_k, int n_docs, int H, int D, int kp, int64_t P, int Kp,
+                        const int64_t *rows, int64_t n_rows, int32_t *sel, double *sel_score,
+                        double *kth, double *kth_cond, int32_t *n_sel)
 {
     ora_operands o;
     ops_init(&o, q, qs, w, pk, pks, fp8, H, D, P);
     int32_t *cu_pools = (int32_t *)malloc(sizeof(int32_t) * (n_docs + 1));
-    ora_cu_pools(cu_seqlens, n_docs, kp, cu_pools);
+    ora_cu_pools(cu_k, n_docs, kp, cu_pools);
+    ora_layout L = {cu_q, q_pos, cu_k, cu_pools, n_docs};
 #pragma omp parallel
     {
         double *qd = (double *)malloc(sizeof(double) * H * D);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t r = 0; r < n_rows; r++) {
-            int64_t t = rows[r];
-            int doc = doc_of_token(cu_seqlens, n_docs, t);
-            int64_t tau = t - cu_seqlens[doc];
-            int64_t nc = n_complete(tau, kp);
+            int64_t t = rows[r], tau, nc;
+            int doc = layout_row(&L, t, &tau, &nc, kp);
             cand *c = (cand *)malloc(sizeof(cand) * (nc > 0 ? nc : 1));
             double *conds = (double *)malloc(sizeof(double) * (nc > 0 ? nc : 1));
             double *scores = (double *)malloc(sizeof(double) * (nc > 0 ? nc : 1));
@@ -504,6 +538,16 @@ void ora_select_rows(const void *q, const float *qs, const float *w, const void 
     }
     free(cu_pools);
     ops_free(&o);
+}
+
+void ora_select_rows(const void *q, const float *qs, const float *w, const void *pk,
+                     const float *pks, int fp8, const int32_t *cu_seqlens, int n_docs,
+                     int H, int D, int kp, int64_t P, int Kp, const int64_t *rows, int64_t n_rows,
+                     int32_t *sel, double *sel_score, double *kth, double *kth_cond,
+                     int32_t *n_sel)
+{
+    ora_select_rows_at(q, qs, w, pk, pks, fp8, cu_seqlens, NULL, cu_seqlens, n_docs, H, D, kp, P,
+                       Kp, rows, n_rows, sel, sel_score, kth, kth_cond, n_sel);
 }
 
 /* Full score rows (small cases): out[r, p] for every global pool p, -inf
@@ -553,30 +597,38 @@ void ora_score_rows_full(const void *q, const float *qs, const float *w, const v
  *   the tail tokens t-((tau+1) mod kp)+1 .. t when tail is on and the query's
  *   own pool is incomplete, then -1 padding.  sel holds the pool lists
  *   [n_rows, Kp] (global pools, -1 padded). */
-void ora_expand_rows(const int32_t *sel, const int32_t *cu_seqlens, int n_docs, int kp, int Kp,
-                     int tail, const int64_t *rows, int64_t n_rows, int32_t *out)
+void ora_expand_rows_at(const int32_t *sel, const int32_t *cu_q, const int32_t *q_pos,
+                        const int32_t *cu_k, int n_docs, int kp, int Kp, int tail,
+                        const int64_t *rows, int64_t n_rows, int32_t *out)
 {
     int64_t W = (int64_t)Kp * kp + kp - 1;
     int32_t *cu_pools = (int32_t *)malloc(sizeof(int32_t) * (n_docs + 1));
-    ora_cu_pools(cu_seqlens, n_docs, kp, cu_pools);
+    ora_cu_pools(cu_k, n_docs, kp, cu_pools);
+    ora_layout L = {cu_q, q_pos, cu_k, cu_pools, n_docs};
     for (int64_t r = 0; r < n_rows; r++) {
-        int64_t t = rows[r];
-        int doc = doc_of_token(cu_seqlens, n_docs, t);
-        int64_t tau = t - cu_seqlens[doc];
+        int64_t t = rows[r], tau, nc;
+        int doc = layout_row(&L, t, &tau, &nc, kp);
         int64_t pos = 0;
         for (int64_t i = 0; i < Kp; i++) {
             int32_t g = sel[r * Kp + i];
             if (g < 0) continue;
             int64_t j = g - cu_pools[doc];
-            for (int s = 0; s < kp; s++) out[r * W + pos++] = (int32_t)(cu_seqlens[doc] + j * kp + s);
+            for (int s = 0; s < kp; s++) out[r * W + pos++] = (int32_t)(cu_k[doc] + j * kp + s);
         }
         if (tail) {
             int64_t rem = (tau + 1) % kp;
-            for (int64_t i = rem - 1; i >= 0; i--) out[r * W + pos++] = (int32_t)(t - i);
+            for (int64_t i = rem - 1; i >= 0; i--)
+                out[r * W + pos++] = (int32_t)(cu_k[doc] + tau - i);
         }
         while (pos < W) out[r * W + pos++] = -1;
     }
     free(cu_pools);
+}
+
+void ora_expand_rows(const int32_t *sel, const int32_t *cu_seqlens, int n_docs, int kp, int Kp,
+                     int tail, const int64_t *rows, int64_t n_rows, int32_t *out)
+{
+    ora_expand_rows_at(sel, cu_seqlens, NULL, cu_seqlens, n_docs, kp, Kp, tail, rows, n_rows, out);
 }
 
 int ora_num_threads(void)

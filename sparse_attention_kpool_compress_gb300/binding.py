@@ -50,6 +50,9 @@ _SIGS = {
     "kpool_score_dense": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I,
                                _P, _P, _SZ, _P]),
     "kpool_expand_indices": (_I, [_P, _P, _P, _I, _L, _I, _I, _I, _P, _P]),
+    "kpool_score_topk_at": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I, _I,
+                                 _P, _P, _P, _SZ, _P]),
+    "kpool_expand_indices_at": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _P, _P]),
     "kpool_read_status": (_I, [_P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -263,6 +266,48 @@ def kpool_expand_indices(pool_idx, kpool: int, index_topk: int, always_select_ta
     _check(_lib.kpool_expand_indices(_ptr(pool_idx), _ptr(cu_seqlens), _ptr(cu_pools), n_docs, T,
                                      kpool, index_topk, int(bool(always_select_tail)), _ptr(tok),
                                      _stream(pool_idx.device)), "kpool_expand_indices")
+    return tok
+
+
+def kpool_score_topk_at(q, w, pk, kpool: int, index_topk: int, cu_seqlens_q, q_start_pos,
+                        cu_pools, q_scale=None, pk_scale=None, workspace=None, out=None):
+    """Positioned queries (decode / chunked prefill): document d's query rows
+    [cu_seqlens_q[d], cu_seqlens_q[d+1]) sit at positions q_start_pos[d] + i."""
+    fp8, n_docs, T, H, D, P = _score_common(q, w, pk, q_scale, pk_scale, cu_seqlens_q, cu_pools)
+    _need(q_start_pos, "q_start_pos", torch.int32)
+    Kp = index_topk // kpool
+    if workspace is None:
+        workspace = new_workspace(T, H, n_docs, q.device)
+    if out is None:
+        idx = torch.empty(T, Kp, dtype=torch.int32, device=q.device)
+        sc = torch.empty(T, Kp, dtype=torch.float32, device=q.device)
+    else:
+        idx, sc = out
+    _check(_lib.kpool_score_topk_at(_ptr(_as_u8(q)) if fp8 else _ptr(q), _ptr(q_scale), _ptr(w),
+                                    _ptr(_as_u8(pk)) if fp8 else _ptr(pk), _ptr(pk_scale),
+                                    _ptr(cu_seqlens_q), _ptr(q_start_pos), _ptr(cu_pools), n_docs,
+                                    T, P, H, D, kpool, index_topk, int(fp8), _ptr(idx), _ptr(sc),
+                                    _ptr(workspace), workspace.numel(), _stream(q.device)),
+           "kpool_score_topk_at")
+    return idx, sc
+
+
+def kpool_expand_indices_at(pool_idx, kpool: int, index_topk: int, cu_seqlens_q, q_start_pos,
+                            cu_seqlens_k, cu_pools, always_select_tail: bool = True, out=None):
+    """Key-token indices for positioned queries [Tq, Kp*kpool + kpool - 1]."""
+    _need(pool_idx, "pool_idx", torch.int32)
+    for t_, n_ in ((cu_seqlens_q, "cu_seqlens_q"), (q_start_pos, "q_start_pos"),
+                   (cu_seqlens_k, "cu_seqlens_k"), (cu_pools, "cu_pools")):
+        _need(t_, n_, torch.int32)
+    T = pool_idx.shape[0]
+    Kp = index_topk // kpool
+    W = Kp * kpool + kpool - 1
+    tok = out if out is not None else torch.empty(T, W, dtype=torch.int32, device=pool_idx.device)
+    _check(_lib.kpool_expand_indices_at(_ptr(pool_idx), _ptr(cu_seqlens_q), _ptr(q_start_pos),
+                                        _ptr(cu_seqlens_k), _ptr(cu_pools), cu_seqlens_q.numel() - 1,
+                                        T, kpool, index_topk, int(bool(always_select_tail)),
+                                        _ptr(tok), _stream(pool_idx.device)),
+           "kpool_expand_indices_at")
     return tok
 
 

@@ -284,6 +284,74 @@ int kpool_score_topk_noalloc(const void *q, const float *q_scale, const float *w
                             scratch_bytes, stream);
 }
 
+int kpool_score_topk_at(const void *q, const float *q_scale, const float *w, const void *pk,
+                        const float *pk_scale, const int32_t *cu_seqlens_q,
+                        const int32_t *q_start_pos, const int32_t *cu_pools, int n_docs,
+                        int64_t Tq, int64_t P_total, int H, int D, int kpool, int index_topk,
+                        int fp8, int32_t *pool_idx_out, float *pool_score_out, void *workspace,
+                        size_t workspace_bytes, kpool_stream_t stream)
+{
+    clear_error();
+    if (!cu_seqlens_q || !q_start_pos || !cu_pools)
+        return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens_q, q_start_pos and cu_pools are required");
+    if (!aligned(q_start_pos, 4)) return fail(KPOOL_ERR_INVALID_ARG, "q_start_pos misaligned");
+    // the key-side pool count is independent of the number of query rows
+    int rc = check_score_args(q, q_scale, w, pk, pk_scale, cu_seqlens_q, cu_pools, n_docs, Tq, 0,
+                              H, D, kpool, fp8, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (P_total < 0) return fail(KPOOL_ERR_INVALID_ARG, "P_total < 0");
+    if (P_total > 0 && !pk) return fail(KPOOL_ERR_INVALID_ARG, "pk must be non-NULL");
+    if (index_topk < 1 || index_topk % kpool != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
+    const int Kp = index_topk / kpool;
+    const int cap = score_capacity(H, D, fp8);
+    int kp2 = 1;
+    while (kp2 < Kp) kp2 <<= 1;
+    if (Kp + 128 > cap || kp2 > cap)
+        return fail(KPOOL_ERR_UNSUPPORTED,
+                    "index_topk / kpool = %d exceeds the per-query candidate capacity %d for H=%d",
+                    Kp, cap, H);
+    if (Tq > 0 && (!pool_idx_out || !pool_score_out))
+        return fail(KPOOL_ERR_INVALID_ARG, "pool_idx_out and pool_score_out must be non-NULL");
+    ScoreArgs a{};
+    a.q = q; a.q_scale = q_scale; a.w = w; a.pk = pk; a.pk_scale = pk_scale;
+    a.cu_seqlens = cu_seqlens_q; a.cu_pools = cu_pools; a.q_pos = q_start_pos; a.n_docs = n_docs;
+    a.T = Tq; a.P_total = P_total; a.H = H; a.D = D; a.kpool = kpool; a.Kp = Kp;
+    a.fp8 = fp8 ? 1 : 0; a.mode = 0;
+    a.pool_idx = pool_idx_out; a.pool_score = pool_score_out; a.scores = nullptr;
+    a.ws = static_cast<int *>(workspace); a.ws_bytes = workspace_bytes;
+    return run_score(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kpool_expand_indices_at(const int32_t *pool_idx, const int32_t *cu_seqlens_q,
+                            const int32_t *q_start_pos, const int32_t *cu_seqlens_k,
+                            const int32_t *cu_pools, int n_docs, int64_t Tq, int kpool,
+                            int index_topk, int always_select_tail, int32_t *tok_idx_out,
+                            kpool_stream_t stream)
+{
+    clear_error();
+    int rc = check_common(Tq, kpool);
+    if (rc) return rc;
+    if (!cu_seqlens_q || !q_start_pos || !cu_seqlens_k || !cu_pools)
+        return fail(KPOOL_ERR_INVALID_ARG,
+                    "cu_seqlens_q, q_start_pos, cu_seqlens_k and cu_pools are required");
+    if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1");
+    if (!aligned(cu_seqlens_q, 4) || !aligned(q_start_pos, 4) || !aligned(cu_seqlens_k, 4) ||
+        !aligned(cu_pools, 4))
+        return fail(KPOOL_ERR_INVALID_ARG, "index arrays must be 4-byte aligned");
+    if (index_topk < 1 || index_topk % kpool != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
+    if (Tq > 0 && (!pool_idx || !tok_idx_out))
+        return fail(KPOOL_ERR_INVALID_ARG, "pool_idx and tok_idx_out must be non-NULL");
+    if (!aligned(pool_idx, 4) || !aligned(tok_idx_out, 4))
+        return fail(KPOOL_ERR_INVALID_ARG, "pool_idx and tok_idx_out must be 4-byte aligned");
+    const int Kp = index_topk / kpool;
+    KPOOL_CUDA_CHECK(launch_expand(pool_idx, cu_seqlens_q, q_start_pos, cu_seqlens_k, cu_pools,
+                                   n_docs, Tq, kpool, Kp, always_select_tail ? 1 : 0, tok_idx_out,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+    return KPOOL_OK;
+}
+
 int kpool_score_dense(const void *q, const float *q_scale, const float *w, const void *pk,
                       const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
                       int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool, int fp8,
@@ -326,8 +394,8 @@ int kpool_expand_indices(const int32_t *pool_idx, const int32_t *cu_seqlens,
     const int Kp = index_topk / kpool;
     if (static_cast<int64_t>(Kp) * kpool + kpool > 0x7FFFFFFF)
         return fail(KPOOL_ERR_UNSUPPORTED, "row width overflows");
-    KPOOL_CUDA_CHECK(launch_expand(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp,
-                                   always_select_tail ? 1 : 0, tok_idx_out,
+    KPOOL_CUDA_CHECK(launch_expand(pool_idx, cu_seqlens, nullptr, nullptr, cu_pools, n_docs, T,
+                                   kpool, Kp, always_select_tail ? 1 : 0, tok_idx_out,
                                    reinterpret_cast<cudaStream_t>(stream)));
     return KPOOL_OK;
 }

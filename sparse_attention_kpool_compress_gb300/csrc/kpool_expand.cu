@@ -30,6 +30,7 @@ constexpr int kStageInts = 512;   // per-warp staging of a row's pool list (larg
 template <int KP>   // KP > 0: compile-time kpool; 0: runtime kp
 __global__ void __launch_bounds__(kThreads) expand_kernel(
     const int32_t *__restrict__ pool_idx, const int32_t *__restrict__ cu_seqlens,
+    const int32_t *__restrict__ q_pos, const int32_t *__restrict__ cu_k,
     const int32_t *__restrict__ cu_pools, int n_docs, int64_t T, int kp_rt, int Kp, int tail,
     int32_t *__restrict__ out)
 {
@@ -39,18 +40,21 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + wib;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
-    int64_t doc_start = 0, pool_lo = 0, pool_hi = T / kp;
+    // query row t: document d, position tau, keys starting at token key0
+    int64_t doc_start = 0, key0 = 0, pos0 = 0, pool_lo = 0, pool_hi = T / kp;
     if (cu_seqlens != nullptr) {
         const int d = doc_of_token(cu_seqlens, n_docs, t);
         doc_start = cu_seqlens[d];
+        key0 = cu_k != nullptr ? cu_k[d] : doc_start;
+        pos0 = q_pos != nullptr ? q_pos[d] : 0;
         pool_lo = cu_pools[d];
         pool_hi = cu_pools[d + 1];
     }
-    const int64_t tau = t - doc_start;
-    const int64_t nc = (tau + 1) / kp;
+    const int64_t tau = pos0 + (t - doc_start);
+    const int64_t nc = min((tau + 1) / kp, pool_hi - pool_lo);
     const int n_sel = static_cast<int>(nc < Kp ? nc : Kp);
     const int n_pool_tok = n_sel * kp;
-    const int n_tail = tail ? static_cast<int>((tau + 1) - nc * kp) : 0;
+    const int n_tail = tail ? static_cast<int>((tau + 1) % kp) : 0;   // own incomplete pool
     const int W = Kp * kp + kp - 1;
     const int32_t *row_in = pool_idx + t * Kp;
     int32_t *row_out = out + t * W;
@@ -68,9 +72,9 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(
             const int s = c - e * kp;
             const int32_t g = staged ? st[e] : row_in[e];
             if (g >= pool_lo && g < pool_hi)
-                v = static_cast<int32_t>(doc_start + (g - pool_lo) * kp + s);
+                v = static_cast<int32_t>(key0 + (g - pool_lo) * kp + s);
         } else if (c < n_pool_tok + n_tail) {
-            v = static_cast<int32_t>(t - n_tail + 1 + (c - n_pool_tok));
+            v = static_cast<int32_t>(key0 + tau - n_tail + 1 + (c - n_pool_tok));
         }
         __stcs(row_out + c, v);   // streaming store: the table is not re-read here
     }
@@ -79,17 +83,18 @@ __global__ void __launch_bounds__(kThreads) expand_kernel(
 }  // namespace
 
 cudaError_t launch_expand(const int32_t *pool_idx, const int32_t *cu_seqlens,
-                          const int32_t *cu_pools, int n_docs, int64_t T, int kpool, int Kp,
-                          int tail, int32_t *tok_idx, cudaStream_t s)
+                          const int32_t *q_pos, const int32_t *cu_k, const int32_t *cu_pools,
+                          int n_docs, int64_t T, int kpool, int Kp, int tail, int32_t *tok_idx,
+                          cudaStream_t s)
 {
     if (T == 0) return cudaSuccess;
     const unsigned blocks = static_cast<unsigned>((T + kRowsPerBlock - 1) / kRowsPerBlock);
     switch (kpool) {
-    case 1: expand_kernel<1><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
-    case 2: expand_kernel<2><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
-    case 4: expand_kernel<4><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
-    case 8: expand_kernel<8><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
-    default: expand_kernel<0><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    case 1: expand_kernel<1><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, q_pos, cu_k, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    case 2: expand_kernel<2><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, q_pos, cu_k, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    case 4: expand_kernel<4><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, q_pos, cu_k, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    case 8: expand_kernel<8><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, q_pos, cu_k, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
+    default: expand_kernel<0><<<blocks, kThreads, 0, s>>>(pool_idx, cu_seqlens, q_pos, cu_k, cu_pools, n_docs, T, kpool, Kp, tail, tok_idx); break;
     }
     return cudaGetLastError();
 }

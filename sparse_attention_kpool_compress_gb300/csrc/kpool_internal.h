@@ -43,8 +43,9 @@ cudaError_t launch_compress(const void *k, const void *gate, const float *ape,
 cudaError_t launch_quantize_fp8(const void *x, int64_t rows, uint8_t *out, float *scale,
                                 cudaStream_t s);
 cudaError_t launch_expand(const int32_t *pool_idx, const int32_t *cu_seqlens,
-                          const int32_t *cu_pools, int n_docs, int64_t T, int kpool, int Kp,
-                          int tail, int32_t *tok_idx, cudaStream_t s);
+                          const int32_t *q_pos, const int32_t *cu_k, const int32_t *cu_pools,
+                          int n_docs, int64_t T, int kpool, int Kp, int tail, int32_t *tok_idx,
+                          cudaStream_t s);
 
 // Scoring (kpool_score.cu).  mode 0 = top-k, 1 = dense scores.
 struct ScoreArgs {
@@ -55,6 +56,7 @@ struct ScoreArgs {
     const float *pk_scale;
     const int32_t *cu_seqlens;
     const int32_t *cu_pools;
+    const int32_t *q_pos;    // per-document position of the first query row (NULL = 0)
     int n_docs;
     int64_t T;
     int64_t P_total;

@@ -116,7 +116,7 @@ Layout make_layout(int H, int D, int fp8)
     L.scr_off = off;  off += kGroups * 32 * 4 + ((QT * 4 + 15) / 16) * 16;
     L.thr_off = off;  off += ((QT * 4 + 15) / 16) * 16;
     L.bar_off = off;  off += 256;
-    L.ti_off = off;   off += 2 * 16;
+    L.ti_off = off;   off += 2 * 32;
     L.misc_off = off; off += 16;
     const int avail = kSmemLimit - 1024 - static_cast<int>(off);
     int C = avail / (8 * QT);
@@ -135,6 +135,7 @@ struct Params {
     const float *pk_scale;
     const int32_t *cu_seqlens;
     const int32_t *cu_pools;
+    const int32_t *q_pos;     // per-document position of the first query row, or NULL
     int n_docs, T, P_total, kp, Kp, fp8, mode;
     int32_t *pool_idx;
     float *pool_score;
@@ -181,15 +182,19 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
     return __all_sync(kFull, ok);
 }
 
+// A query tile: rows [t0, min(t0 + QT, doc_end)) of the document starting at
+// query row doc_start; row t sits at document-local position
+// pos_base + (t - doc_start) and may see the document's complete pools
+// j < min(floor((pos + 1) / kpool), pool_count), global index pool_base + j.
 struct TileInfo {
-    int t0, doc_start, doc_end, pool_base;
+    int t0, doc_start, doc_end, pool_base, pos_base, pool_count, pad0, pad1;
 };
 
 __device__ __forceinline__ int pool_tiles_of(const TileInfo &ti, int QT, int kp)
 {
-    const int tau0 = ti.t0 - ti.doc_start;
+    const int tau0 = ti.pos_base + (ti.t0 - ti.doc_start);
     const int nq = min(QT, ti.doc_end - ti.t0);
-    const int nc_last = (tau0 + nq) / kp;       // (tau_last + 1) / kp
+    const int nc_last = min((tau0 + nq) / kp, ti.pool_count);   // (tau_last + 1) / kp
     return (nc_last + kBM - 1) / kBM;
 }
 
@@ -530,14 +535,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileInfo t;
         const int2 e = reinterpret_cast<const int2 *>(p.ws + WS_TABLE_INTS)[tile];
         t.t0 = e.x;
+        t.pad0 = t.pad1 = 0;
+        t.pos_base = p.q_pos != nullptr ? p.q_pos[e.y] : 0;
         if (p.cu_seqlens != nullptr) {
             t.doc_start = p.cu_seqlens[e.y];
             t.doc_end = p.cu_seqlens[e.y + 1];
             t.pool_base = p.cu_pools[e.y];
+            t.pool_count = p.cu_pools[e.y + 1] - p.cu_pools[e.y];
         } else {
             t.doc_start = 0;
             t.doc_end = p.T;
             t.pool_base = 0;
+            t.pool_count = p.P_total;
         }
         return t;
     };
@@ -569,7 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 TileInfo t;
                 if (tile >= ntiles) {
                     t.t0 = -1;
-                    t.doc_start = t.doc_end = t.pool_base = 0;
+                    t.doc_start = t.doc_end = t.pool_base = t.pos_base = t.pool_count = 0;
+                    t.pad0 = t.pad1 = 0;
                 } else {
                     t = tile_info(tile);
                 }
@@ -736,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(BTI_EMPTY + slot));
             if (t.t0 < 0) break;
-            const int tau0 = t.t0 - t.doc_start;
+            const int tau0 = t.pos_base + (t.t0 - t.doc_start);
             const int nq = min(QT, t.doc_end - t.t0);
             const int npt = pool_tiles_of(t, QT, p.kp);
 
@@ -759,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < QS; ++j) {
                 thr[j] = 0u;
-                nc[j] = (tau0 + qbase + j + 1) / p.kp;
+                nc[j] = min((tau0 + qbase + j + 1) / p.kp, t.pool_count);
             }
             bool aborted = false;
 
@@ -905,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     n = Kp;
                 }
                 const int64_t row = static_cast<int64_t>(t.t0 + q) * Kp;
-                const int nc_q = (tau0 + q + 1) / p.kp;   // local pools visible to q
+                const int nc_q = min((tau0 + q + 1) / p.kp, t.pool_count);   // visible local pools
                 const int words = (nc_q + 31) / 32;
                 if (words <= C - n) {
                     group_rank_store(csq, ciq, n, t.pool_base, words, g, gtid, gs,
@@ -1161,6 +1171,7 @@ int run_score(const ScoreArgs &a, cudaStream_t s)
     prm.pk_scale = a.pk_scale;
     prm.cu_seqlens = a.cu_seqlens;
     prm.cu_pools = a.cu_pools;
+    prm.q_pos = a.q_pos;
     prm.n_docs = a.n_docs;
     prm.T = static_cast<int>(a.T);
     prm.P_total = static_cast<int>(a.P_total);

@@ -1,0 +1,109 @@
+"""Positioned queries (decode and chunked prefill): kpool_score_topk_at and
+kpool_expand_indices_at against the oracle's select_rows_at / expand_rows_at,
+and against the rows of a full prefill computed by the GPU itself."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_kpool_compress_gb300 import workloads as W
+from kpool_checks import check_selection
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_attention_kpool_compress_gb300 as K
+    return K
+
+
+def _bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def _keys(seed=3):
+    wl = W.Workload("kv", T=6000, H=64, D=128, kpool=4, index_topk=512, n_docs=3,
+                    doc_len_range=(1000, 3000))
+    inp = W.make_inputs(wl, seed=seed)
+    return wl, inp, inp.cu_seqlens.numpy()
+
+
+def _run(K, ora, wl, inp, cu_k, chunks):
+    """chunks: per document (a, b) document-local query positions [a, b)."""
+    dev = torch.device("cuda")
+    kp, Kp = wl.kpool, wl.Kp
+    pkb = ora.compress(W.bits(inp.k), W.bits(inp.gate), inp.ape.numpy(), cu_k, kp)
+    cu_pools_h, P = K.kpool_num_pools(torch.from_numpy(cu_k), wl.T, kp)
+    rows = np.concatenate([np.arange(cu_k[d] + a, cu_k[d] + b) for d, (a, b) in enumerate(chunks)])
+    cq = np.concatenate([[0], np.cumsum([b - a for a, b in chunks])]).astype(np.int32)
+    qpos = np.array([a for a, _ in chunks], np.int32)
+    q = inp.q[torch.from_numpy(rows)].contiguous()
+    w = inp.w[torch.from_numpy(rows)].contiguous()
+    d_cq, d_qpos = torch.from_numpy(cq).to(dev), torch.from_numpy(qpos).to(dev)
+    d_cp, d_ck = cu_pools_h.to(dev), torch.from_numpy(cu_k).to(dev)
+    idx, sc = K.kpool_score_topk_at(q.to(dev), w.to(dev), _bf16(pkb).to(dev), kp, wl.index_topk,
+                                    d_cq, d_qpos, d_cp)
+    tok = K.kpool_expand_indices_at(idx, kp, wl.index_topk, d_cq, d_qpos, d_ck, d_cp, True)
+    torch.cuda.synchronize()
+    ops = ora.Operands(W.bits(q), w.numpy(), pkb)
+    return rows, cq, qpos, pkb, ops, idx.cpu().numpy(), sc.cpu().numpy(), tok.cpu().numpy()
+
+
+def _check_vs_oracle(ora, ops, cq, qpos, cu_k, wl, idx, sc, tok):
+    n = idx.shape[0]
+    o = ora.select_rows_at(ops, cq, qpos, cu_k, wl.kpool, wl.Kp, np.arange(n))
+    # reuse the generic checker through a small adapter over the _at oracle
+    class At:
+        select_rows = staticmethod(lambda ops_, cu, kp, Kp, rows: ora.select_rows_at(
+            ops_, cq, qpos, cu_k, kp, Kp, rows))
+        score_pairs = staticmethod(lambda ops_, cu, kp, rows, pools: ora.score_pairs_at(
+            ops_, cq, qpos, cu_k, kp, rows, pools))
+    st = check_selection(At, ops, None, wl.kpool, wl.Kp, np.arange(n), idx, sc, TOL, "at")
+    want = ora.expand_rows_at(idx, cq, qpos, cu_k, wl.kpool, wl.Kp, True, np.arange(n))
+    assert np.array_equal(tok, want)
+    return o, st
+
+
+def test_chunked_prefill(K, ora):
+    wl, inp, cu_k = _keys()
+    L = np.diff(cu_k)
+    chunks = [(int(L[d] // 3), int(2 * L[d] // 3)) for d in range(3)]
+    rows, cq, qpos, pkb, ops, idx, sc, tok = _run(K, ora, wl, inp, cu_k, chunks)
+    _check_vs_oracle(ora, ops, cq, qpos, cu_k, wl, idx, sc, tok)
+    # the same rows of a GPU full prefill are identical, bit for bit
+    dev = torch.device("cuda")
+    cu_pools_h, _ = K.kpool_num_pools(torch.from_numpy(cu_k), wl.T, wl.kpool)
+    fidx, fsc = K.kpool_score_topk(inp.q.to(dev), inp.w.to(dev), _bf16(pkb).to(dev), wl.kpool,
+                                   wl.index_topk, torch.from_numpy(cu_k).to(dev),
+                                   cu_pools_h.to(dev))
+    ftok = K.kpool_expand_indices(fidx, wl.kpool, wl.index_topk, True,
+                                  torch.from_numpy(cu_k).to(dev), cu_pools_h.to(dev))
+    torch.cuda.synchronize()
+    assert np.array_equal(fidx.cpu().numpy()[rows], idx)
+    assert np.array_equal(fsc.cpu().numpy()[rows], sc)
+    assert np.array_equal(ftok.cpu().numpy()[rows], tok)
+
+
+def test_decode_one_query_per_document(K, ora):
+    wl, inp, cu_k = _keys(seed=4)
+    L = np.diff(cu_k)
+    chunks = [(int(L[d] - 1), int(L[d])) for d in range(3)]
+    rows, cq, qpos, pkb, ops, idx, sc, tok = _run(K, ora, wl, inp, cu_k, chunks)
+    o, _ = _check_vs_oracle(ora, ops, cq, qpos, cu_k, wl, idx, sc, tok)
+    assert np.all(o["n_sel"] == np.minimum(L // wl.kpool, wl.Kp))
+
+
+def test_positioned_small_ragged(K, ora):
+    """Tiny documents, chunks at the start, the middle and a ragged tail."""
+    wl = W.Workload("kv2", T=700, H=16, D=64, kpool=4, index_topk=40, n_docs=4,
+                    doc_len_range=(30, 400))
+    inp = W.make_inputs(wl, seed=9)
+    cu_k = inp.cu_seqlens.numpy()
+    L = np.diff(cu_k)
+    chunks = [(0, int(min(L[0], 5))), (int(L[1] // 2), int(L[1])), (1, 2), (int(L[3] - 7), int(L[3]))]
+    rows, cq, qpos, pkb, ops, idx, sc, tok = _run(K, ora, wl, inp, cu_k, chunks)
+    _check_vs_oracle(ora, ops, cq, qpos, cu_k, wl, idx, sc, tok)

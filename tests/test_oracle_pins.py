@@ -509,3 +509,66 @@ def test_compress_condition_scale(ora):
     kp_ = kb & 0x7FFF
     _, ex2, cond2 = ora.compress(kp_, gb, ape, None, 4, want_cond=True)
     assert np.allclose(cond2, ex2, rtol=1e-15, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# Queries at given positions (decode / chunked prefill)
+# ---------------------------------------------------------------------------
+
+def _thd_case(seed=7):
+    wl = W.Workload("at", T=400, H=3, D=16, kpool=4, index_topk=24, n_docs=3,
+                    doc_len_range=(60, 200))
+    inp = W.make_inputs(wl, seed=seed)
+    cu = inp.cu_seqlens.numpy()
+    pk = None
+    return wl, inp, cu
+
+
+def test_chunked_prefill_equals_full_prefill_rows(ora):
+    """A chunk of query rows [a, b) of each document, given as its own query
+    batch at position offset a - doc_start, gets exactly the plain result of
+    rows [a, b) (selection, scores and expansion to key-token indices)."""
+    wl, inp, cu = _thd_case()
+    kb, gb, qb = W.bits(inp.k), W.bits(inp.gate), W.bits(inp.q)
+    w = inp.w.numpy()
+    pk = ora.compress(kb, gb, inp.ape.numpy(), cu, wl.kpool)
+    full = ora.select_rows(ora.Operands(qb, w, pk), cu, wl.kpool, wl.Kp, np.arange(wl.T))
+    full_tok = ora.expand_rows(full["sel"], cu, wl.T, wl.kpool, wl.Kp, True, np.arange(wl.T))
+    # chunk of each document: its middle third
+    rows, cq, qpos = [], [0], []
+    for d in range(3):
+        L = cu[d + 1] - cu[d]
+        a, b = cu[d] + L // 3, cu[d] + 2 * L // 3
+        rows.extend(range(a, b))
+        cq.append(cq[-1] + (b - a))
+        qpos.append(a - cu[d])
+    rows = np.array(rows)
+    ops_c = ora.Operands(qb[rows], w[rows], pk)
+    got = ora.select_rows_at(ops_c, cq, qpos, cu, wl.kpool, wl.Kp, np.arange(len(rows)))
+    assert np.array_equal(got["sel"], full["sel"][rows])
+    fin = np.isfinite(full["sel_score"][rows])
+    assert np.array_equal(got["sel_score"][fin], full["sel_score"][rows][fin])
+    tok = ora.expand_rows_at(got["sel"], cq, qpos, cu, wl.kpool, wl.Kp, True,
+                             np.arange(len(rows)))
+    assert np.array_equal(tok, full_tok[rows])
+    sc, cd = ora.score_pairs_at(ops_c, cq, qpos, cu, wl.kpool, [0, 0], [0, cu[-1] // 4])
+    assert np.isneginf(sc[1])     # another document's pool is not visible
+
+
+def test_decode_queries_see_their_document_prefix(ora):
+    """One decode query per document at its last position equals the last row
+    of the plain result; a position past the keys sees every pool (clamped)."""
+    wl, inp, cu = _thd_case(seed=8)
+    kb, gb, qb = W.bits(inp.k), W.bits(inp.gate), W.bits(inp.q)
+    w = inp.w.numpy()
+    pk = ora.compress(kb, gb, inp.ape.numpy(), cu, wl.kpool)
+    last = cu[1:] - 1
+    full = ora.select_rows(ora.Operands(qb, w, pk), cu, wl.kpool, wl.Kp, last)
+    cq = np.arange(4, dtype=np.int32)
+    qpos = (cu[1:] - cu[:-1] - 1).astype(np.int32)
+    ops_d = ora.Operands(qb[last], w[last], pk)
+    got = ora.select_rows_at(ops_d, cq, qpos, cu, wl.kpool, wl.Kp, np.arange(3))
+    assert np.array_equal(got["sel"], full["sel"])
+    far = ora.select_rows_at(ops_d, cq, qpos + 1000, cu, wl.kpool, 1000, np.arange(3))
+    cp = ora.cu_pools(cu, wl.kpool)
+    assert list(far["n_sel"]) == list(np.diff(cp))
