@@ -189,6 +189,39 @@ def oracle_sample(inp, rows, n_threads=None):
     return dt, ora.num_threads()
 
 
+def positioned_rows(inp, n, seed=1):
+    """Query rows of a positioned workload timed on the oracle: all of them
+    when there are at most n, else n drawn without replacement."""
+    if inp.Tq <= n:
+        return np.arange(inp.Tq, dtype=np.int64)
+    g = torch.Generator().manual_seed(seed)
+    return torch.sort(torch.randperm(inp.Tq, generator=g)[:n]).values.numpy().astype(np.int64)
+
+
+def oracle_sample_at(inp, rows, pk=None):
+    """Time the oracle as it stands on positioned query rows: for a chunk of
+    one sequence, compression of the chunk's pools; then selection and
+    expansion of the rows against the pooled keys of their documents."""
+    import oracle as ora
+    ora.build()
+    wl = inp.wl
+    cu_k = inp.cu_seqlens.numpy()
+    cq, qp = inp.cu_q.numpy(), inp.q_pos.numpy()
+    kb, gb = W.bits(inp.k), W.bits(inp.gate)
+    if pk is None:
+        pk = ora.compress(kb, gb, inp.ape.numpy(), cu_k if len(cu_k) > 2 else None, wl.kpool)
+    plan = chunk_compress_plan(inp)
+    t0 = time.perf_counter()
+    if plan is not None:
+        pk = pk.copy()
+        pk[plan[1]:] = ora.compress(kb[plan[0]:], gb[plan[0]:], inp.ape.numpy(), None, wl.kpool)
+    ops = ora.Operands(W.bits(inp.q), inp.w.numpy(), pk)
+    o = ora.select_rows_at(ops, cq, qp, cu_k, wl.kpool, wl.Kp, rows)
+    ora.expand_rows_at(o["sel"], cq, qp, cu_k, wl.kpool, wl.Kp, wl.tail, rows)
+    dt = time.perf_counter() - t0
+    return dt, ora.num_threads()
+
+
 def baseline_rows(wl, n, seed=1):
     g = torch.Generator().manual_seed(seed)
     return torch.sort(torch.randperm(wl.T, generator=g)[:n]).values.numpy().astype(np.int64)
@@ -201,18 +234,33 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     inp = W.make_inputs(wl)
-    rows = baseline_rows(wl, args.ref_rows)
+    if wl.queries != "all":
+        import oracle as ora
+        ora.build()
+        cu_k = inp.cu_seqlens.numpy()
+        pk = ora.compress(W.bits(inp.k), W.bits(inp.gate), inp.ape.numpy(),
+                          cu_k if len(cu_k) > 2 else None, wl.kpool)
+        rows = positioned_rows(inp, args.ref_rows)
+        sample_fn = lambda r: oracle_sample_at(inp, r, pk)   # noqa: E731
+        sample = ("%d query rows of %s per step (selection and expansion of the rows over the "
+                  "pooled-key cache%s)" % (len(rows), wl.name,
+                                           "; compression of the chunk's pools"
+                                           if chunk_compress_plan(inp) else ""))
+    else:
+        rows = baseline_rows(wl, args.ref_rows)
+        sample_fn = lambda r: oracle_sample(inp, r)   # noqa: E731
+        sample = ("%d uniformly drawn query rows of %s per step (compression of all %d pools, "
+                  "selection and expansion of the rows)" % (len(rows), wl.name,
+                                                            wl.T // wl.kpool))
     for _ in range(args.warmup):
-        oracle_sample(inp, rows[: max(1, len(rows) // 8)])
+        sample_fn(rows[: max(1, len(rows) // 8)])
     times = []
     cores = 1
     for _ in range(args.steps):
-        dt, cores = oracle_sample(inp, rows)
+        dt, cores = sample_fn(rows)
         times.append(dt)
     ms = 1000.0 * sum(times) / len(times)
     value = len(rows) / (ms / 1000.0)
-    sample = ("%d uniformly drawn query rows of %s per step (compression of all %d pools, "
-              "selection and expansion of the rows)" % (len(rows), wl.name, wl.T // wl.kpool))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -225,6 +273,46 @@ def run_reference(args, wl):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def timed_loop(step, n_seg, steps, stream, in_bytes, local, barrier):
+    """Time ``steps`` calls of ``step(events)`` with CUDA events on ``stream``.
+
+    ``step`` records ``n_seg + 1`` events (segment boundaries).  When the
+    bytes a step reads are below 512 MiB, L2 (129 MB) is flushed before
+    every step by writing a 512 MiB buffer and the step time is the mean of
+    the per-step events; otherwise it is the whole region / steps.  Returns
+    (ms per step, [mean ms per segment], clocks, note on L2)."""
+    dev = torch.device("cuda", local)
+    flush = None
+    if in_bytes < 512 * 2 ** 20:
+        flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_seg + 1)]
+           for _ in range(steps)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        step(evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    if flush is None:
+        ms_step = e0.elapsed_time(e1) / steps
+        note = "inputs larger than L2 (%.2f GiB read per step)" % (in_bytes / 2 ** 30)
+    else:
+        ms_step = statistics.mean(e[0].elapsed_time(e[n_seg]) for e in evs)
+        note = ("L2 flushed between timed steps (512 MiB write); step time = mean of "
+                "per-step CUDA events")
+    segs = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(n_seg)]
+    return ms_step, segs, clocks, note
 
 
 def main():
@@ -260,6 +348,8 @@ def main():
 
     dev = torch.device("cuda", local)
     inp = W.make_inputs(wl)
+    if wl.queries != "all":
+        return run_positioned(args, wl, inp, K, dev, world, rank, local)
     T, H, D, kp, topk, Kp = wl.T, wl.H, wl.D, wl.kpool, wl.index_topk, wl.Kp
     multi = inp.cu_seqlens.numel() > 2
     if multi:
@@ -340,35 +430,9 @@ def main():
     if status != 0:
         raise RuntimeError("device status %d after warm-up" % status)
 
-    # inputs smaller than L2 (129 MB on GB300) are flushed from it between timed
-    # steps by writing a 512 MiB buffer; each step then has its own events
     in_bytes = sum(x.numel() * x.element_size() for x in (q, k, gate, w))
-    flush = None
-    if in_bytes < 256 * 2 ** 20:
-        flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
-    sampler = ClockSampler(local)
-    sampler.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier()
-    e0.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        step(evs[i])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop()
-    if flush is None:
-        ms_step = e0.elapsed_time(e1) / args.steps
-    else:
-        ms_step = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
-    t_compress = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    t_score = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    t_expand = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    ms_step, (t_compress, t_score, t_expand), clocks, l2_note = timed_loop(
+        step, 3, args.steps, stream, in_bytes, local, barrier)
     ms_step = job_time_ms(ms_step, world, dev)
     status = K.kpool_read_status(ws)
     if status != 0:
@@ -452,11 +516,212 @@ def main():
             "config": {"workload": wl.name, "desc": wl.desc, "T": T, "H": H, "D": D,
                        "kpool": kp, "index_topk": topk, "tail": wl.tail, "fp8": wl.fp8,
                        "parallelism": "replicas" if world > 1 else "single",
-                       "l2": ("inputs larger than L2 (q alone %.2f GiB)"
-                              % (q.numel() * q.element_size() / 2 ** 30)) if flush is None else
-                             "L2 flushed between timed steps (512 MiB write); step time = mean "
-                             "of per-step CUDA events"},
+                       "l2": l2_note},
             "scoring_tflops": achieved,
+            "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "kernels": side,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def positioned_counts(inp):
+    """Per query row: complete causal pools n_c and the document's pool count."""
+    wl = inp.wl
+    cu_k = inp.cu_seqlens.numpy().astype(np.int64)
+    cq = inp.cu_q.numpy().astype(np.int64)
+    qp = inp.q_pos.numpy().astype(np.int64)
+    nc = np.empty(inp.Tq, np.int64)
+    for d in range(len(qp)):
+        tau = qp[d] + np.arange(cq[d + 1] - cq[d])
+        nc[cq[d]:cq[d + 1]] = np.minimum((tau + 1) // wl.kpool, (cu_k[d + 1] - cu_k[d]) // wl.kpool)
+    return nc
+
+
+def chunk_compress_plan(inp):
+    """A chunked prefill of one sequence whose chunk starts on a pool boundary
+    re-compresses the chunk's keys into the pooled-key cache each step:
+    (first key token, first pool).  None when the step compresses nothing
+    (decode: the pooled-key cache is resident)."""
+    wl = inp.wl
+    if not wl.queries.startswith("chunk:") or inp.cu_seqlens.numel() != 2:
+        return None
+    p0 = int(inp.q_pos[0])
+    if p0 % wl.kpool:
+        return None
+    return p0, p0 // wl.kpool
+
+
+def run_positioned(args, wl, inp, K, dev, world, rank, local):
+    """Decode and chunked-prefill steps: kpool_score_topk_at and
+    kpool_expand_indices_at over a resident pooled-key cache (plus, for a
+    chunk, the compression of the chunk's own keys into that cache)."""
+    T, H, D, kp, topk, Kp = wl.T, wl.H, wl.D, wl.kpool, wl.index_topk, wl.Kp
+    Tq = inp.Tq
+    n_docs = inp.cu_seqlens.numel() - 1
+    cu_pools_h, P = K.kpool_num_pools(inp.cu_seqlens, T, kp)
+    cu_k, cp = inp.cu_seqlens.to(dev), cu_pools_h.to(dev)
+    cq, qp = inp.cu_q.to(dev), inp.q_pos.to(dev)
+    q, w = inp.q.to(dev), inp.w.to(dev)
+    k, gate, ape = inp.k.to(dev), inp.gate.to(dev), inp.ape.to(dev)
+    # the pooled-key cache: every complete pool of every document
+    pk = K.kpool_compress(k, gate, ape, kp, cu_k if n_docs > 1 else None,
+                          cp if n_docs > 1 else None, P)
+    plan = chunk_compress_plan(inp)
+    if plan is not None:
+        kc, gc = k[plan[0]:], gate[plan[0]:]
+        pkc = pk[plan[1]:]
+    else:
+        del k, gate
+    pool_idx = torch.empty(Tq, Kp, dtype=torch.int32, device=dev)
+    pool_score = torch.empty(Tq, Kp, dtype=torch.float32, device=dev)
+    Wd = Kp * kp + kp - 1
+    tok = torch.empty(Tq, Wd, dtype=torch.int32, device=dev)
+    ws = K.new_workspace(Tq, H, n_docs, dev)
+    stream = torch.cuda.current_stream(dev)
+    B = K.binding
+    L = B._lib
+    sp = B._stream(dev)
+
+    def chk(rc, name):
+        if rc != 0:
+            raise B.KPoolError(rc, name)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if plan is not None:
+            chk(L.kpool_compress(B._ptr(kc), B._ptr(gc), B._ptr(ape), None, None, 1,
+                                 kc.shape[0], D, kp, kc.shape[0] // kp, B._ptr(pkc), None, None,
+                                 sp), "kpool_compress")
+        if ev is not None:
+            ev[1].record(stream)
+        chk(L.kpool_score_topk_at(B._ptr(q), None, B._ptr(w), B._ptr(pk), None, B._ptr(cq),
+                                  B._ptr(qp), B._ptr(cp), n_docs, Tq, P, H, D, kp, topk, 0,
+                                  B._ptr(pool_idx), B._ptr(pool_score), B._ptr(ws), ws.numel(),
+                                  sp), "kpool_score_topk_at")
+        if ev is not None:
+            ev[2].record(stream)
+        chk(L.kpool_expand_indices_at(B._ptr(pool_idx), B._ptr(cq), B._ptr(qp), B._ptr(cu_k),
+                                      B._ptr(cp), n_docs, Tq, kp, topk, int(wl.tail),
+                                      B._ptr(tok), sp), "kpool_expand_indices_at")
+        if ev is not None:
+            ev[3].record(stream)
+
+    launches_per_step = (1 if plan is not None else 0) + 2 + 1
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if K.kpool_read_status(ws) != 0:
+        raise RuntimeError("device status %d after warm-up" % K.kpool_read_status(ws))
+    nc = positioned_counts(inp)
+    # algorithmic bytes of kpool_score_topk_at: each document's visible pooled
+    # keys once, the queries, head weights and the selected (index, score) rows
+    vis = np.zeros(n_docs, np.int64)
+    cqh = inp.cu_q.numpy()
+    for d in range(n_docs):
+        if cqh[d + 1] > cqh[d]:
+            vis[d] = nc[cqh[d + 1] - 1]
+    score_bytes = int(vis.sum()) * D * 2 + Tq * H * D * 2 + Tq * H * 4 + Tq * Kp * 8
+    in_bytes = score_bytes + ((T - plan[0]) * D * 4 if plan is not None else 0)
+    ms_step, (t_compress, t_score, t_expand), clocks, l2_note = timed_loop(
+        step, 3, args.steps, stream, in_bytes, local, barrier)
+    ms_step = job_time_ms(ms_step, world, dev)
+    if K.kpool_read_status(ws) != 0:
+        raise RuntimeError("device status %d after the timed steps" % K.kpool_read_status(ws))
+
+    # ---- end to end through the public API from pinned host memory --------
+    e2e = None
+    if not args.no_e2e:
+        hq, hw = inp.q.pin_memory(), inp.w.pin_memory()
+        hsrc = [hq, hw]
+        if plan is not None:
+            hk, hg = inp.k[plan[0]:].pin_memory(), inp.gate[plan[0]:].pin_memory()
+            hsrc += [hk, hg]
+        htok = torch.empty(Tq, Wd, dtype=torch.int32).pin_memory()
+        dsts = [torch.empty_like(x, device=dev) for x in hsrc]
+        h2d = sum(x.numel() * x.element_size() for x in hsrc)
+        d2h = htok.numel() * htok.element_size()
+
+        def e2e_step():
+            for d_, h_ in zip(dsts, hsrc):
+                d_.copy_(h_, non_blocking=True)
+            if plan is not None:
+                K.kpool_compress(dsts[2], dsts[3], ape, kp, out=pkc)
+            idx, _ = K.kpool_score_topk_at(dsts[0], dsts[1], pk, kp, topk, cq, qp, cp,
+                                           workspace=ws)
+            tk = K.kpool_expand_indices_at(idx, kp, topk, cq, qp, cu_k, cp, wl.tail)
+            htok.copy_(tk, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        n_e2e = max(2, min(args.steps, 10))
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = job_time_ms(a0.elapsed_time(a1) / n_e2e, world, dev)
+        e2e = {"value": whole_job_rate(Tq, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
+               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peaks, peak_src = load_peaks()
+    flops = 2.0 * H * D * float(nc.sum())
+    tflops = flops / (t_score / 1000.0) / 1e12
+    gbs = score_bytes / (t_score / 1000.0) / 1e9
+    t_tensor = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = score_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops_sustained"],
+                    "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops_sustained"],
+                    "peak_source": "bf16 sustained (%s)" % peak_src}
+    else:
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "peak_source": "hbm copy (%s)" % peak_src}
+    roofline.update({"kernel": "kpool_score_topk_at", "traffic": recorded_traffic(
+        "kpool_score_topk_at", wl.name), "algorithmic_flops_per_launch": flops,
+        "algorithmic_bytes_per_launch": score_bytes, "scoring_tflops": tflops,
+        "scoring_gbs": gbs, "causal_pairs": int(nc.sum()), "ms_per_launch": t_score,
+        "roofline_ms": max(t_tensor, t_hbm) * 1000.0})
+    side = {"compress_ms": t_compress if plan is not None else None,
+            "expand_ms": t_expand,
+            "expand_gbs": (Tq * Kp * 4 + Tq * Wd * 4) / (t_expand / 1000.0) / 1e9,
+            "score_topk_ms": t_score, "score_queries_per_s": Tq / (t_score / 1000.0)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rows = positioned_rows(inp, args.baseline_rows)
+        dt, cores = oracle_sample_at(inp, rows)
+        cpu = {"value": len(rows) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%d query rows of %s (selection and expansion of those rows%s), %.1f s"
+                         % (len(rows), wl.name, ", compression of the chunk's pools"
+                            if plan is not None else "", dt)}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": whole_job_rate(Tq, world, ms_step), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "desc": wl.desc, "T_keys": T, "T_queries": Tq,
+                       "H": H, "D": D, "kpool": kp, "index_topk": topk, "tail": wl.tail,
+                       "fp8": False, "queries": wl.queries,
+                       "step": ("kpool_compress (the chunk's keys) + " if plan is not None else
+                                "pooled-key cache resident; ") +
+                               "kpool_score_topk_at + kpool_expand_indices_at",
+                       "parallelism": "replicas" if world > 1 else "single", "l2": l2_note},
+            "scoring_tflops": tflops,
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "kernels": side,
         }

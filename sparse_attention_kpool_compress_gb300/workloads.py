@@ -8,10 +8,18 @@ inputs from it.  Draw order and distributions (seed 0 by default, a
 1. document lengths (packed-THD workloads only): ``u_i ~ U[lo, hi)`` in
    float64, ``L_i = floor(u_i * T / sum(u))``, the remainder added to the
    last document;
-2. ``q [T, H, D]``, 3. ``k [T, D]``, 4. ``gate [T, D]``: N(0, 1) drawn in
+2. ``q [Tq, H, D]``, 3. ``k [T, D]``, 4. ``gate [T, D]``: N(0, 1) drawn in
    float32 and rounded to bfloat16 by torch;
 5. ``ape [kpool, D]``: N(0, 0.1^2) float32;
-6. ``w [T, H]``: N(0, 1) / sqrt(H) float32.
+6. ``w [Tq, H]``: N(0, 1) / sqrt(H) float32.
+
+``T`` counts key tokens.  A prefill (``queries="all"``) has one query per
+key, ``Tq = T``.  Positioned workloads have fewer queries, the last ones of
+each document: ``"last"`` is one decode query per document (at the document's
+last key), ``"chunk:N"`` the final chunk of N tokens of a chunked prefill.
+Their query rows are described by ``cu_q`` (query row offsets per document)
+and ``q_pos`` (position, inside the document's keys, of each document's first
+query).
 
 Large tensors are drawn in row chunks of ``CHUNK_ELEMS`` elements so that the
 float32 staging buffer stays small; the chunking is part of the definition.
@@ -40,6 +48,7 @@ class Workload:
     equal_docs: bool = False              # batch of equal sequences
     fp8: bool = False
     seed: int = 0
+    queries: str = "all"                  # "all" | "last" | "chunk:N"
     desc: str = ""
 
     @property
@@ -63,6 +72,18 @@ WORKLOADS = {
                           n_docs=2, equal_docs=True, fp8=True,
                           desc="FP8 indexer mode: 2 sequences of 32768 tokens, H=64 D=128 "
                                "kpool=4 index_topk=2048, E4M3 scoring"),
+    "chunk_16k_of_128k": Workload("chunk_16k_of_128k", T=131072, H=64, D=128, kpool=4,
+                                  index_topk=2048, queries="chunk:16384",
+                                  desc="Chunked prefill: the last 16384-token chunk of a "
+                                       "131072-token sequence (queries at positions "
+                                       "114688..131071 over all 131072 keys), H=64 D=128 "
+                                       "kpool=4 index_topk=2048"),
+    "decode_128x32k": Workload("decode_128x32k", T=128 * 32768, H=64, D=128, kpool=4,
+                               index_topk=2048, n_docs=128, doc_len_range=(8192, 57344),
+                               queries="last",
+                               desc="Decode: one query per sequence at its last key, 128 "
+                                    "sequences with lengths U[8192,57344] rescaled to "
+                                    "4194304 keys, H=64 D=128 kpool=4 index_topk=2048"),
 }
 
 
@@ -95,16 +116,41 @@ def _normal_bf16(shape, gen, scale=1.0):
     return out.view(*shape)
 
 
+def query_layout(queries: str, lens: list):
+    """Per-document query counts and first positions of a positioned
+    workload, or None for a prefill."""
+    if queries == "all":
+        return None
+    if queries == "last":
+        n = [1 if L > 0 else 0 for L in lens]
+    elif queries.startswith("chunk:"):
+        c = int(queries.split(":", 1)[1])
+        n = [min(c, L) for L in lens]
+    else:
+        raise ValueError("unknown query layout %r" % queries)
+    cu_q = [0]
+    for x in n:
+        cu_q.append(cu_q[-1] + x)
+    q_pos = [L - x for L, x in zip(lens, n)]
+    return cu_q, q_pos
+
+
 @dataclass
 class Inputs:
     wl: Workload
-    cu_seqlens: torch.Tensor      # int32 [n_docs + 1]
-    q: torch.Tensor               # bf16 [T, H, D]
+    cu_seqlens: torch.Tensor      # int32 [n_docs + 1] (key tokens)
+    q: torch.Tensor               # bf16 [Tq, H, D]
     k: torch.Tensor               # bf16 [T, D]
     gate: torch.Tensor            # bf16 [T, D]
     ape: torch.Tensor             # fp32 [kpool, D]
-    w: torch.Tensor               # fp32 [T, H]
+    w: torch.Tensor               # fp32 [Tq, H]
+    cu_q: torch.Tensor | None = None     # int32 [n_docs + 1], positioned workloads
+    q_pos: torch.Tensor | None = None    # int32 [n_docs], positioned workloads
     extra: dict = field(default_factory=dict)
+
+    @property
+    def Tq(self) -> int:
+        return self.q.shape[0]
 
 
 def make_inputs(wl: Workload, seed: int | None = None, T: int | None = None) -> Inputs:
@@ -120,12 +166,17 @@ def make_inputs(wl: Workload, seed: int | None = None, T: int | None = None) -> 
     for L in lens:
         cu.append(cu[-1] + L)
     cu_seqlens = torch.tensor(cu, dtype=torch.int32)
-    q = _normal_bf16((wl.T, wl.H, wl.D), gen)
+    lay = query_layout(wl.queries, lens)
+    Tq = wl.T if lay is None else lay[0][-1]
+    q = _normal_bf16((Tq, wl.H, wl.D), gen)
     k = _normal_bf16((wl.T, wl.D), gen)
     gate = _normal_bf16((wl.T, wl.D), gen)
     ape = torch.randn(wl.kpool, wl.D, generator=gen, dtype=torch.float32) * 0.1
-    w = torch.randn(wl.T, wl.H, generator=gen, dtype=torch.float32) / math.sqrt(wl.H)
-    return Inputs(wl, cu_seqlens, q, k, gate, ape, w)
+    w = torch.randn(Tq, wl.H, generator=gen, dtype=torch.float32) / math.sqrt(wl.H)
+    if lay is None:
+        return Inputs(wl, cu_seqlens, q, k, gate, ape, w)
+    return Inputs(wl, cu_seqlens, q, k, gate, ape, w,
+                  torch.tensor(lay[0], dtype=torch.int32), torch.tensor(lay[1], dtype=torch.int32))
 
 
 def sample_rows(T: int, n_sample: int = 1024, edge: int = 64, seed: int = 0,

@@ -107,3 +107,56 @@ def test_positioned_small_ragged(K, ora):
     chunks = [(0, int(min(L[0], 5))), (int(L[1] // 2), int(L[1])), (1, 2), (int(L[3] - 7), int(L[3]))]
     rows, cq, qpos, pkb, ops, idx, sc, tok = _run(K, ora, wl, inp, cu_k, chunks)
     _check_vs_oracle(ora, ops, cq, qpos, cu_k, wl, idx, sc, tok)
+
+
+def _fullsize(K, ora, name, n_sample):
+    """The positioned workload at full size in the benchmark's launch
+    configuration: pooled keys (GPU vs oracle), the scorer on the oracle's
+    pooled keys for sampled query rows, and bit-exact expansion."""
+    from kpool_checks import bf16_bits, check_pooled_keys
+    dev = torch.device("cuda")
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    cu_k = inp.cu_seqlens.numpy()
+    multi = len(cu_k) > 2
+    cu_pools_h, P = K.kpool_num_pools(inp.cu_seqlens, wl.T, wl.kpool)
+    d_ck, d_cp = inp.cu_seqlens.to(dev), cu_pools_h.to(dev)
+    pk = K.kpool_compress(inp.k.to(dev), inp.gate.to(dev), inp.ape.to(dev), wl.kpool,
+                          d_ck if multi else None, d_cp if multi else None, P)
+    pkb, exact, cond = ora.compress(W.bits(inp.k), W.bits(inp.gate), inp.ape.numpy(),
+                                    cu_k if multi else None, wl.kpool, want_exact=True,
+                                    want_cond=True)
+    check_pooled_keys(bf16_bits(pk), pkb, exact, cond, name)
+    cq, qp = inp.cu_q.numpy(), inp.q_pos.numpy()
+    d_cq, d_qp = inp.cu_q.to(dev), inp.q_pos.to(dev)
+    q, w = inp.q.to(dev), inp.w.to(dev)
+    idx, sc = K.kpool_score_topk_at(q, w, _bf16(pkb).to(dev), wl.kpool, wl.index_topk, d_cq, d_qp,
+                                    d_cp)
+    tok = K.kpool_expand_indices_at(idx, wl.kpool, wl.index_topk, d_cq, d_qp, d_ck, d_cp, True)
+    torch.cuda.synchronize()
+    rows = W.sample_rows(inp.Tq, n_sample).numpy()
+    idx_h, sc_h, tok_h = idx.cpu().numpy(), sc.cpu().numpy(), tok.cpu().numpy()
+    ops = ora.Operands(W.bits(inp.q), inp.w.numpy(), pkb)
+
+    class At:
+        select_rows = staticmethod(lambda ops_, cu, kp, Kp, r: ora.select_rows_at(
+            ops_, cq, qp, cu_k, kp, Kp, r))
+        score_pairs = staticmethod(lambda ops_, cu, kp, r, p: ora.score_pairs_at(
+            ops_, cq, qp, cu_k, kp, r, p))
+    check_selection(At, ops, None, wl.kpool, wl.Kp, rows, idx_h[rows], sc_h[rows], TOL, name)
+    want = ora.expand_rows_at(idx_h[rows], cq, qp, cu_k, wl.kpool, wl.Kp, True, rows)
+    assert np.array_equal(tok_h[rows], want)
+    return inp, idx_h
+
+
+@pytest.mark.slow
+def test_fullsize_chunk_16k_of_128k(K, ora):
+    inp, idx = _fullsize(K, ora, "chunk_16k_of_128k", 512)
+    # every chunk query sees more complete pools than the budget
+    assert np.all(idx >= 0)
+
+
+@pytest.mark.slow
+def test_fullsize_decode_128x32k(K, ora):
+    inp, idx = _fullsize(K, ora, "decode_128x32k", 1024)   # 128 rows: all of them
+    assert inp.Tq == 128 and np.all(idx >= 0)
