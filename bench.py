@@ -579,7 +579,7 @@ def run_positioned(args, wl, inp, K, dev, world, rank, local):
     pool_score = torch.empty(Tq, Kp, dtype=torch.float32, device=dev)
     Wd = Kp * kp + kp - 1
     tok = torch.empty(Tq, Wd, dtype=torch.int32, device=dev)
-    ws = K.new_workspace(Tq, H, n_docs, dev)
+    ws = K.new_workspace(Tq, H, n_docs, dev, kp, topk)
     stream = torch.cuda.current_stream(dev)
     B = K.binding
     L = B._lib

@@ -141,6 +141,22 @@ KPOOL_API int kpool_quantize_fp8(const void *x, int64_t rows, int D, uint8_t *x_
 KPOOL_API size_t kpool_score_topk_workspace_size(int64_t T, int H, int n_docs);
 
 /*
+ * kpool_score_topk_workspace_size_split -- bytes of a workspace that also
+ * lets kpool_score_topk / kpool_score_topk_at split long pool lists over
+ * several CTAs when a call has few query tiles (decode batches, short
+ * chunks: at most 1024 tiles of 256 / H rows).  Each query tile's pools are
+ * then scored in units on different SMs; every unit keeps its own best Kp
+ * (the same scores, the same order: score descending, ties to the lower
+ * pool index) and the last unit to finish merges them, so the outputs are
+ * identical to the unsplit schedule's.  Equal to
+ * kpool_score_topk_workspace_size(T, H, n_docs) when the call is not
+ * eligible; 0 for unsupported arguments.  A workspace at least this large
+ * enables the split schedule; a smaller valid one runs unsplit.
+ */
+KPOOL_API size_t kpool_score_topk_workspace_size_split(int64_t T, int H, int n_docs, int kpool,
+                                                       int index_topk);
+
+/*
  * kpool_score_topk -- causal pool scoring fused with top-k selection
  * (Megatron-LM PR section 3: top-k over index_topk // kpool pools; xtuner
  * PR: relu homogeneity lets any head_dim^-0.5 factor live in w).
@@ -160,9 +176,11 @@ KPOOL_API size_t kpool_score_topk_workspace_size(int64_t T, int H, int n_docs);
  *   q            bf16 [T, H, D] (or E4M3), 16-byte aligned
  *   w            fp32 [T, H]
  *   pk           bf16 [P_total, D] (or E4M3), 16-byte aligned
- *   workspace    >= kpool_score_topk_workspace_size(T, H, n_docs) bytes,
- *                256-byte aligned; its contents are overwritten.  Calls that
- *                share one workspace must not overlap on the device.
+ *   workspace    >= kpool_score_topk_workspace_size(T, H, n_docs) bytes
+ *                (kpool_score_topk_workspace_size_split for the split-pool
+ *                schedule), 256-byte aligned; its contents are overwritten.
+ *                Calls that share one workspace must not overlap on the
+ *                device.
  * Supported: H in {4, 8, 16, 32, 64, 128}; D in {32, 64, 128} (128 in FP8
  * mode); Kp <= a per-H capacity (UNSUPPORTED beyond it).
  * Device-side: cu_seqlens is validated by the schedule kernel; on failure
@@ -186,7 +204,9 @@ KPOOL_API int kpool_score_topk(const void *q, const float *q_scale, const float 
  * to the document's pools.  With q_start_pos = 0 and the keys' cu_seqlens as
  * cu_seqlens_q this is kpool_score_topk.  All three index arrays are device
  * int32 and required; Tq = cu_seqlens_q[n_docs]; the workspace is sized by
- * kpool_score_topk_workspace_size(Tq, H, n_docs).  Outputs as in
+ * kpool_score_topk_workspace_size(Tq, H, n_docs), or by
+ * kpool_score_topk_workspace_size_split(Tq, H, n_docs, kpool, index_topk)
+ * to let a decode batch spread each document's pools over the SMs.  Outputs as in
  * kpool_score_topk (global pool indices, ascending).
  */
 KPOOL_API int kpool_score_topk_at(const void *q, const float *q_scale, const float *w,

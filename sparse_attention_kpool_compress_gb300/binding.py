@@ -43,6 +43,7 @@ _SIGS = {
     "kpool_compress": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _L, _P, _P, _P, _P]),
     "kpool_quantize_fp8": (_I, [_P, _L, _I, _P, _P, _P]),
     "kpool_score_topk_workspace_size": (_SZ, [_L, _I, _I]),
+    "kpool_score_topk_workspace_size_split": (_SZ, [_L, _I, _I, _I, _I]),
     "kpool_score_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I, _I,
                               _P, _P, _P, _SZ, _P]),
     "kpool_score_topk_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I,
@@ -177,8 +178,19 @@ def kpool_score_topk_workspace_size(T: int, H: int, n_docs: int = 1) -> int:
     return int(_lib.kpool_score_topk_workspace_size(T, H, n_docs))
 
 
-def new_workspace(T: int, H: int, n_docs: int = 1, device="cuda") -> torch.Tensor:
-    n = kpool_score_topk_workspace_size(T, H, n_docs)
+def kpool_score_topk_workspace_size_split(T: int, H: int, n_docs: int, kpool: int,
+                                          index_topk: int) -> int:
+    return int(_lib.kpool_score_topk_workspace_size_split(T, H, n_docs, kpool, index_topk))
+
+
+def new_workspace(T: int, H: int, n_docs: int = 1, device="cuda", kpool: int | None = None,
+                  index_topk: int | None = None) -> torch.Tensor:
+    """Workspace for kpool_score_topk[_at]; with kpool and index_topk it is
+    large enough for the split-pool schedule of calls with few query tiles."""
+    if kpool is not None and index_topk is not None:
+        n = kpool_score_topk_workspace_size_split(T, H, n_docs, kpool, index_topk)
+    else:
+        n = kpool_score_topk_workspace_size(T, H, n_docs)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
@@ -205,7 +217,7 @@ def kpool_score_topk(q, w, pk, kpool: int, index_topk: int, cu_seqlens=None, cu_
     fp8, n_docs, T, H, D, P = _score_common(q, w, pk, q_scale, pk_scale, cu_seqlens, cu_pools)
     Kp = index_topk // kpool
     if workspace is None:
-        workspace = new_workspace(T, H, n_docs, q.device)
+        workspace = new_workspace(T, H, n_docs, q.device, kpool, index_topk)
     if out is None:
         idx = torch.empty(T, Kp, dtype=torch.int32, device=q.device)
         sc = torch.empty(T, Kp, dtype=torch.float32, device=q.device)
@@ -277,7 +289,7 @@ def kpool_score_topk_at(q, w, pk, kpool: int, index_topk: int, cu_seqlens_q, q_s
     _need(q_start_pos, "q_start_pos", torch.int32)
     Kp = index_topk // kpool
     if workspace is None:
-        workspace = new_workspace(T, H, n_docs, q.device)
+        workspace = new_workspace(T, H, n_docs, q.device, kpool, index_topk)
     if out is None:
         idx = torch.empty(T, Kp, dtype=torch.int32, device=q.device)
         sc = torch.empty(T, Kp, dtype=torch.float32, device=q.device)

@@ -218,6 +218,14 @@ size_t kpool_score_topk_workspace_size(int64_t T, int H, int n_docs)
     return score_workspace_bytes(T, H, n_docs);
 }
 
+size_t kpool_score_topk_workspace_size_split(int64_t T, int H, int n_docs, int kpool,
+                                             int index_topk)
+{
+    if (T < 0 || n_docs < 1 || check_h(H) != KPOOL_OK) return 0;
+    if (kpool < 1 || index_topk < 1 || index_topk % kpool != 0) return 0;
+    return score_workspace_split_bytes(T, H, n_docs, index_topk / kpool);
+}
+
 int kpool_score_topk(const void *q, const float *q_scale, const float *w, const void *pk,
                      const float *pk_scale, const int32_t *cu_seqlens, const int32_t *cu_pools,
                      int n_docs, int64_t T, int64_t P_total, int H, int D, int kpool,

@@ -68,6 +68,9 @@ struct ScoreArgs {
     size_t ws_bytes;
 };
 size_t score_workspace_bytes(int64_t T, int H, int n_docs);
+// Bytes that also hold the split-pool schedule's tables and partial lists
+// (equal to score_workspace_bytes when the call cannot use it).
+size_t score_workspace_split_bytes(int64_t T, int H, int n_docs, int Kp);
 int score_capacity(int H, int D, int fp8);   // candidate slots per query (0 = unsupported)
 int run_score(const ScoreArgs &a, cudaStream_t s);
 // Query tiles the fixed scratch of kpool_score_topk_noalloc can schedule.

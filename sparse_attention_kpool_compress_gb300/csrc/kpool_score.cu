@@ -25,6 +25,8 @@
 // the lower pool index by position and no final sort is needed.
 #include <cuda.h>
 
+#include <algorithm>
+#include <type_traits>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -52,6 +54,13 @@ constexpr int kGroupThreads = 32 * kGroupWarps;       // 128
 constexpr int kSlack = 64;                            // extra entries a mid-stream prune may keep
 // register split (setmaxnreg): 128 threads x 32 + 512 x 112 = 640 x 96 (launch budget)
 constexpr int kRegsOther = 32, kRegsEpi = 112;
+// split-pool schedule (few query tiles with long pool lists: decode, short
+// chunks): a query tile's pool tiles are cut into units scored by different
+// CTAs, whose best-Kp lists the last unit to finish merges
+constexpr int kSplitMaxQT = 1024;                     // query tiles it schedules, at most
+constexpr int64_t kSplitEntries = int64_t(1) << 21;   // (index, score) entries of partial lists
+constexpr int kSplitMaxSplits = 16;                   // units per query tile, at most
+constexpr int kSplitMinTiles = 4;                     // pool tiles per unit, at least
 
 // Optional phase timers (build with -DKPOOL_PHASE_TIMERS): per-role cycle
 // counts of waits and work, summed over all CTAs into g_phase_timers and read
@@ -116,7 +125,7 @@ Layout make_layout(int H, int D, int fp8)
     L.scr_off = off;  off += kGroups * 32 * 4 + ((QT * 4 + 15) / 16) * 16;
     L.thr_off = off;  off += ((QT * 4 + 15) / 16) * 16;
     L.bar_off = off;  off += 256;
-    L.ti_off = off;   off += 2 * 32;
+    L.ti_off = off;   off += 3 * 64;   // two producer slots + the epilogue's current unit
     L.misc_off = off; off += 16;
     const int avail = kSmemLimit - 1024 - static_cast<int>(off);
     int C = avail / (8 * QT);
@@ -141,6 +150,12 @@ struct Params {
     float *pool_score;
     float *scores;
     int *ws;
+    // split-pool schedule (units == NULL: one unit per query tile)
+    int *units;          // [n_units][8]: t0, doc, i0, i1, slot_base, splits, tile, k
+    int *tile_ctr;       // per query tile: units finished
+    int *part_cnt;       // [slot][QT] entries in each partial list
+    int32_t *part_idx;   // [slot][QT][Kp]
+    float *part_score;   // [slot][QT][Kp]
     uint32_t q_tx, pk_tx, idesc;
     Layout L;
 };
@@ -182,12 +197,18 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
     return __all_sync(kFull, ok);
 }
 
-// A query tile: rows [t0, min(t0 + QT, doc_end)) of the document starting at
-// query row doc_start; row t sits at document-local position
-// pos_base + (t - doc_start) and may see the document's complete pools
+// A unit of work: pool tiles [i0, i1) of the query tile of rows
+// [t0, min(t0 + QT, doc_end)) of the document starting at query row
+// doc_start; row t sits at document-local position pos_base + (t - doc_start)
+// and may see the document's complete pools
 // j < min(floor((pos + 1) / kpool), pool_count), global index pool_base + j.
+// A query tile split into `splits` > 1 units has them at table positions
+// slot_base .. slot_base + splits - 1 (also their partial-list slots); this
+// is unit k; `tile` indexes its arrival counter.
 struct TileInfo {
-    int t0, doc_start, doc_end, pool_base, pos_base, pool_count, pad0, pad1;
+    int t0, doc_start, doc_end, pool_base, pos_base, pool_count;
+    int i0, i1, slot_base, splits, tile, k;
+    int pad[4];
 };
 
 __device__ __forceinline__ int pool_tiles_of(const TileInfo &ti, int QT, int kp)
@@ -476,13 +497,127 @@ __device__ void group_sort_by_pool(float *cs, int *ci, int n, int g, int gtid)
     }
 }
 
-template <int H>
+// Best k (score descending, ties to the lower pool index) of the n entries
+// of sc/ix in global memory (read through L2; padding entries carry index
+// INT_MAX and score -inf), written to cs/ci[0..) in any order; all real
+// entries when at most k of the n_real are real.  One group.  Returns the
+// number written (min(k, n_real)).
+__device__ int group_select_into(const float *sc, const int32_t *ix, int n, int k, int n_real,
+                                 float *cs, int *ci, int g, int gtid, int *hist, int *gs)
+{
+    const int lane = gtid & 31;
+    const bool all = n_real <= k;
+    uint32_t kth = 0u, ithr = 0xFFFFFFFFu;
+    bool edge = false;
+    if (!all) {
+        int above, inbin;
+        radix_kth(n, k, [&](int e) { return fkey(__ldcg(sc + e)); }, [](int) { return true; },
+                  false, 0, g, gtid, hist, gs, kth, above, inbin, edge);
+        if (!edge && above + inbin > k) {
+            uint32_t ik;
+            int iab, iin;
+            bool ied;
+            group_bar(g);   // gs reuse
+            radix_kth(n, k - above, [&](int e) { return ~static_cast<uint32_t>(__ldcg(ix + e)); },
+                      [&](int e) { return fkey(__ldcg(sc + e)) == kth; }, false, 0, g, gtid, hist,
+                      gs, ik, iab, iin, ied);
+            ithr = ~ik;
+        }
+    }
+    group_bar(g);
+    if (gtid == 0) gs[24] = 0;
+    group_bar(g);
+    for (int c = 0; c < n; c += kGroupThreads) {
+        const int e = c + gtid;
+        bool keep = false;
+        float sv = 0.f;
+        int iv = 0;
+        if (e < n) {
+            sv = __ldcg(sc + e);
+            iv = __ldcg(ix + e);
+            const uint32_t key = fkey(sv);
+            keep = all ? iv != 0x7FFFFFFF
+                       : (edge ? key >= kth
+                               : (key > kth || (key == kth && static_cast<uint32_t>(iv) <= ithr)));
+        }
+        const unsigned kb = __ballot_sync(kFull, keep);
+        int base = 0;
+        if (lane == 0 && kb != 0u) base = atomicAdd(&gs[24], __popc(kb));
+        base = __shfl_sync(kFull, base, 0);
+        if (keep) {
+            const int d = base + __popc(kb & ((1u << lane) - 1u));
+            cs[d] = sv;
+            ci[d] = iv;
+        }
+    }
+    group_bar(g);
+    const int total = gs[24];
+    group_bar(g);   // gs reuse
+    return total;
+}
+
+// End of one unit of a split query tile (epilogue threads): its best Kp per
+// query (padded to Kp) go to the tile's partial lists, [query][unit][Kp]; the
+// unit that finishes the tile last selects the best Kp of their union (each
+// of the tile's best Kp lies among the best Kp of its own unit) into its
+// candidate areas and returns true.  Kept out of line: the main loop's code
+// is faster without it.
+__device__ __noinline__ bool split_unit_end(const TileInfo *tu, int nq, int QT, int Kp, int C,
+                                            float *cs, int *ci, int *qcnt, uint32_t *thr_s,
+                                            int *hist, int *gs, int g, int gtid, int etid,
+                                            uint32_t *flag, int32_t *part_idx, float *part_score,
+                                            int *part_cnt, int *tile_ctr)
+{
+    const int splits = tu->splits;
+    const int uk = tu->k;
+    const int64_t tbase = static_cast<int64_t>(tu->slot_base) * QT;
+    for (int q = g; q < nq; q += kGroups) {
+        int n = qcnt[q];
+        float *csq = cs + q * C;
+        int *ciq = ci + q * C;
+        if (n > Kp) {
+            group_select(csq, ciq, n, Kp, true, 0, g, gtid, hist, gs, &thr_s[q]);
+            n = Kp;
+        }
+        const int64_t li = tbase + q * splits + uk;
+        for (int e = gtid; e < Kp; e += kGroupThreads) {
+            const bool real = e < n;
+            part_idx[li * Kp + e] = real ? ciq[e] : 0x7FFFFFFF;
+            part_score[li * Kp + e] = real ? csq[e] : -INFINITY;
+        }
+        if (gtid == 0) part_cnt[li] = n;
+    }
+    __threadfence();
+    ptx::named_bar_sync(1, kEpiThreads);
+    if (etid == 0) *flag = atomicAdd(tile_ctr + tu->tile, 1) == splits - 1 ? 1u : 0u;
+    ptx::named_bar_sync(1, kEpiThreads);
+    const bool last = *flag != 0u;
+    if (last) {
+        __threadfence();
+        for (int q = g; q < nq; q += kGroups) {
+            const int64_t l0 = tbase + q * splits;
+            int n_real = 0;
+            for (int u = 0; u < splits; ++u) n_real += __ldcg(part_cnt + l0 + u);
+            const int n = group_select_into(part_score + l0 * Kp, part_idx + l0 * Kp, splits * Kp,
+                                            Kp, n_real, cs + q * C, ci + q * C, g, gtid, hist, gs);
+            if (gtid == 0) qcnt[q] = n;
+            group_bar(g);
+        }
+    }
+    return last;
+}
+
+// kFew: the instantiation for calls with few query tiles (split-pool schedule,
+// lone-query tiles); the other one carries none of that code, which keeps the
+// main loop of long prefills as fast as it can be compiled.
+template <int H, bool kFew>
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_pk,
                  const __grid_constant__ Params p)
 {
     constexpr int QT = kBN / H;   // queries per tile
-    constexpr int QW = QT / 2;    // queries per epilogue warp
+    // lone-query tiles (decode) pack QT pool tiles per accumulator (H >= 64)
+    constexpr bool kQuad = kFew && H >= 64;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, derived by pointer arithmetic so that every pointer
@@ -532,22 +667,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     Sync sy{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.ws + WS_STATUS};
 
     auto tile_info = [&](int tile) {
-        TileInfo t;
-        const int2 e = reinterpret_cast<const int2 *>(p.ws + WS_TABLE_INTS)[tile];
-        t.t0 = e.x;
-        t.pad0 = t.pad1 = 0;
-        t.pos_base = p.q_pos != nullptr ? p.q_pos[e.y] : 0;
+        TileInfo t{};
+        int d;
+        if (p.units != nullptr) {
+            const int4 *u = reinterpret_cast<const int4 *>(p.units) + 2 * tile;
+            const int4 a = u[0], b = u[1];
+            t.t0 = a.x;
+            d = a.y;
+            t.i0 = a.z;
+            t.i1 = a.w;
+            t.slot_base = b.x;
+            t.splits = b.y;
+            t.tile = b.z;
+            t.k = b.w;
+        } else {
+            const int2 e = reinterpret_cast<const int2 *>(p.ws + WS_TABLE_INTS)[tile];
+            t.t0 = e.x;
+            d = e.y;
+            t.i0 = 0;
+            t.i1 = -1;
+            t.slot_base = -1;
+            t.splits = 1;
+            t.tile = tile;
+        }
+        t.pos_base = p.q_pos != nullptr ? p.q_pos[d] : 0;
         if (p.cu_seqlens != nullptr) {
-            t.doc_start = p.cu_seqlens[e.y];
-            t.doc_end = p.cu_seqlens[e.y + 1];
-            t.pool_base = p.cu_pools[e.y];
-            t.pool_count = p.cu_pools[e.y + 1] - p.cu_pools[e.y];
+            t.doc_start = p.cu_seqlens[d];
+            t.doc_end = p.cu_seqlens[d + 1];
+            t.pool_base = p.cu_pools[d];
+            t.pool_count = p.cu_pools[d + 1] - p.cu_pools[d];
         } else {
             t.doc_start = 0;
             t.doc_end = p.T;
             t.pool_base = 0;
             t.pool_count = p.P_total;
         }
+        if (t.i1 < 0) t.i1 = pool_tiles_of(t, QT, p.kp);
         return t;
     };
 
@@ -575,19 +730,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(bar(BTI_EMPTY + slot), tph ^ 1, sy)) break;
                 PT_MARK(0);
                 const int tile = atomicAdd(p.ws + WS_COUNTER, 1);
-                TileInfo t;
+                TileInfo t{};
                 if (tile >= ntiles) {
                     t.t0 = -1;
-                    t.doc_start = t.doc_end = t.pool_base = t.pos_base = t.pool_count = 0;
-                    t.pad0 = t.pad1 = 0;
                 } else {
                     t = tile_info(tile);
                 }
                 ti_slots[slot] = t;   // published by the mbarrier arrive (release)
                 ptx::mbar_arrive(bar(BTI_FULL + slot));
                 if (t.t0 < 0) break;
-                const int npt = pool_tiles_of(t, QT, p.kp);
-                if (npt == 0) continue;
+                if (t.i1 <= t.i0) continue;
                 PT_MARK(4);
                 if (!wait_bar(bar(BQ_EMPTY), qe_ph ^ 1, sy)) break;
                 PT_MARK(1);
@@ -599,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 q_issued = true;
                 q_issued_ph = qe_ph ^ 1;
                 bool ok = true;
-                for (int i = 0; i < npt; ++i) {
+                for (int i = t.i0; i < t.i1; ++i) {
                     PT_MARK(3);
                     if (!wait_bar(bar(BPK_FULL + S + stage), ph ^ 1, sy)) { ok = false; break; }
                     PT_MARK(2);
@@ -645,21 +797,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TileInfo t = ti_slots[slot];   // after the acquiring wait
                 ptx::mbar_arrive(bar(BTI_EMPTY + slot));
                 if (t.t0 < 0) break;
-                const int npt = pool_tiles_of(t, QT, p.kp);
-                if (npt == 0) continue;
+                const int npt = t.i1 - t.i0;
+                if (npt <= 0) continue;
+                // N = the tile's (query, head) columns, rounded up to 16; a lone
+                // query (decode) packs QT pool tiles into one accumulator, N = H each
+                uint32_t idesc = p.idesc;
+                bool quad = false;
+                if constexpr (kFew) {
+                    const int nqm = min(QT, t.doc_end - t.t0);
+                    quad = kQuad && nqm == 1;
+                    const int ncols = min(kBN, ((nqm * H + 15) / 16) * 16);
+                    idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(ncols >> 3) << 17);
+                }
                 PT_MARK(5);
                 if (!wait_bar(bar(BQ_FULL), qf_ph, sy)) break;
                 PT_MARK(1);
                 qf_ph ^= 1;
                 bool ok = true;
                 for (int i = 0; i < npt; ++i) {
+                    const int sub = quad ? i % QT : 0;   // pool tile's column block
                     PT_MARK(4);
-                    if (!wait_bar(bar(BTM_EMPTY + acc), acc_ph ^ 1, sy)) { ok = false; break; }
+                    if (sub == 0 && !wait_bar(bar(BTM_EMPTY + acc), acc_ph ^ 1, sy)) {
+                        ok = false;
+                        break;
+                    }
                     PT_MARK(2);
                     if (!wait_bar(bar(BPK_FULL + stage), ph, sy)) { ok = false; break; }
                     PT_MARK(3);
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + acc * kAccCols;
+                    const uint32_t d_tmem = tmem_base + acc * kAccCols + sub * H;
                     // descriptors of the K slices: the start-address field advances by
                     // 32 bytes per MMA inside a 128-byte swizzled row, by a chunk
                     // between 128-byte K chunks
@@ -668,22 +834,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.fp8) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            ptx::mma_fp8(d_tmem, ad0 + kk * 2, bd0 + kk * 2, p.idesc, kk != 0);
+                            ptx::mma_fp8(d_tmem, ad0 + kk * 2, bd0 + kk * 2, idesc, kk != 0);
                     } else {
                         for (int c = 0; c < L.n_kchunks; ++c) {
                             const uint64_t ad = ad0 + ((c * L.pk_chunk) >> 4);
                             const uint64_t bd = bd0 + ((c * L.q_chunk) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                ptx::mma_bf16(d_tmem, ad + kk * 2, bd + kk * 2, p.idesc,
+                                ptx::mma_bf16(d_tmem, ad + kk * 2, bd + kk * 2, idesc,
                                               (c | kk) != 0);
                         }
                     }
                     ptx::mma_commit(bar(BPK_FULL + S + stage));
-                    ptx::mma_commit(bar(BTM_FULL + acc));
                     any = true;
                     if (++stage == S) { stage = 0; ph ^= 1; }
-                    if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+                    if (!quad || sub == QT - 1 || i == npt - 1) {
+                        ptx::mma_commit(bar(BTM_FULL + acc));
+                        if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+                    }
                 }
                 ptx::mma_commit(bar(BQ_EMPTY));
                 if (!ok) break;
@@ -743,20 +911,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_bar_warp(bar(BTI_FULL + slot), tph, sy)) break;
             PT_MARK(0);
             const TileInfo t = ti_slots[slot];
+            if (kFew && etid == 0) ti_slots[2] = t;   // for the unit's end (visible after the w barrier)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(BTI_EMPTY + slot));
             if (t.t0 < 0) break;
             const int tau0 = t.pos_base + (t.t0 - t.doc_start);
             const int nq = min(QT, t.doc_end - t.t0);
-            const int npt = pool_tiles_of(t, QT, p.kp);
 
             // the tile's 256 head weights (w, times q_scale in FP8 mode), staged in
             // shared memory once per query tile and read back as broadcasts
+            const bool lone = kQuad && nq == 1;   // its weights fill every query's columns
             if (etid < kBN) {
-                const int qi = etid / H;
+                const int qi = lone ? 0 : etid / H;
                 float v = 0.f;
                 if (qi < nq) {
-                    const int64_t off = static_cast<int64_t>(t.t0) * H + etid;
+                    const int64_t off = static_cast<int64_t>(t.t0) * H + (lone ? etid % H : etid);
                     v = __ldg(p.w + off);
                     if (p.fp8) v *= __ldg(p.q_scale + off);
                 }
@@ -773,22 +942,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool aborted = false;
 
+            // The pool-tile loop.  (Counted from 0: a loop over [i0, i1), or one
+            // with a per-warp branch, compiles to a slower body.)
+            const int npt = t.i1 - t.i0;
+            auto tiles = [&]() {
             for (int i = 0; i < npt; ++i) {
                 PT_MARK(1);
                 if (!wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy)) { aborted = true; break; }
                 PT_MARK(2);
                 ptx::tc_fence_after();
-                const uint32_t tb = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) +
-                                    acc * kAccCols + sl * SLICE;
-                uint32_t v0[32], v1[32];
-                ptx::tmem_ld32(tb, v0);
-                ptx::tmem_ld32(tb + 32, v1);
-                ptx::tmem_ld_wait2(v0, v1);
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
-                if (++acc == 2) { acc = 0; acc_ph ^= 1; }
-
                 // relu(x) * w summed per query over this warp's 64 columns
                 uint64_t a4[QS][NACC];
 #pragma unroll
@@ -810,10 +972,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a4[j][k] = ptx::ffma2(r1, wv.y, a4[j][k]);
                     }
                 };
-                accum(v0, 0);
-                accum(v1, 32);
+                {
+                    const uint32_t tb = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) +
+                                        acc * kAccCols + sl * SLICE;
+                    uint32_t v0[32], v1[32];
+                    ptx::tmem_ld32(tb, v0);
+                    ptx::tmem_ld32(tb + 32, v1);
+                    ptx::tmem_ld_wait2(v0, v1);
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
+                    accum(v0, 0);
+                    accum(v1, 32);
+                }
+                if (++acc == 2) { acc = 0; acc_ph ^= 1; }
 
-                const int pool_local = i * kBM + qr * 32 + lane;
+                const int pool_local = (i + t.i0) * kBM + qr * 32 + lane;
                 const int pool_g = t.pool_base + pool_local;
                 float s[QS];
 #pragma unroll
@@ -897,6 +1071,105 @@ __global__ void __launch_bounds__(kThreads, 1)
                     PT_MARK(5);
                 }
             }
+            };
+            if constexpr (kQuad) {
+                if (nq == 1) {
+                    // A lone query (decode): pool tile m*QT + j sits in the columns of
+                    // query j of accumulator m, so every warp works on the query; its
+                    // candidates may use every query's area (capacity QT * C)
+                    const int nquad = (npt + QT - 1) / QT;
+                    const int nc0 = min((tau0 + 1) / p.kp, t.pool_count);
+                    const int Gq = max(1, min(4, (QT * C - Kp - slack) / (QT * kBM)));
+                    const int room_q = QT * C - Gq * QT * kBM;
+                    uint32_t thr0 = 0u;
+                    for (int m = 0; m < nquad; ++m) {
+                        PT_MARK(1);
+                        if (!wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy)) {
+                            aborted = true;
+                            break;
+                        }
+                        PT_MARK(2);
+                        ptx::tc_fence_after();
+                        uint64_t a4[NACC];
+#pragma unroll
+                        for (int k = 0; k < NACC; ++k) a4[k] = 0ull;
+                        {
+                            const uint32_t tb = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) +
+                                                acc * kAccCols + sl * SLICE;
+                            uint32_t v0[32], v1[32];
+                            ptx::tmem_ld32(tb, v0);
+                            ptx::tmem_ld32(tb + 32, v1);
+                            ptx::tmem_ld_wait2(v0, v1);
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
+#pragma unroll
+                            for (int x = 0; x < 64; x += 4) {
+                                const uint32_t *v = x < 32 ? v0 : v1;
+                                const int xx = x & 31;
+                                const ulonglong2 wv = w4[x / 4];
+                                const uint64_t r0 = ptx::pack_f32x2(
+                                    fmaxf(__uint_as_float(v[xx]), 0.f),
+                                    fmaxf(__uint_as_float(v[xx + 1]), 0.f));
+                                const uint64_t r1 = ptx::pack_f32x2(
+                                    fmaxf(__uint_as_float(v[xx + 2]), 0.f),
+                                    fmaxf(__uint_as_float(v[xx + 3]), 0.f));
+                                a4[(x / 4) % NACC] = ptx::ffma2(r0, wv.x, a4[(x / 4) % NACC]);
+                                a4[(x / 4) % NACC] = ptx::ffma2(r1, wv.y, a4[(x / 4) % NACC]);
+                            }
+                        }
+                        if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+                        float sv = ptx::sum_f32x2(a4[0]);
+#pragma unroll
+                        for (int k = 1; k < NACC; ++k) sv += ptx::sum_f32x2(a4[k]);
+                        if (kHalfQ) {
+                            float *pt = part + (tile_seq & 1) * (4 * kBM);
+                            pt[sl * kBM + qr * 32 + lane] = sv;
+                            ptx::named_bar_sync(1, kEpiThreads);
+                            if (owner) sv += pt[(sl + 1) * kBM + qr * 32 + lane];
+                        }
+                        ++tile_seq;
+                        const int tj = m * QT + qbase;   // this warp's pool tile of the unit
+                        const int pool_local = (t.i0 + tj) * kBM + qr * 32 + lane;
+                        const int pool_g = t.pool_base + pool_local;
+                        if (p.fp8 && pool_g < p.P_total) sv *= p.pk_scale[pool_g];
+                        sv = (sv == 0.f) ? 0.f : sv;   // fold -0 into +0
+                        PT_MARK(3);
+                        if (owner) {
+                            const bool ps = tj < npt && pool_local < nc0 && fkey(sv) > thr0;
+                            const unsigned bal = __ballot_sync(kFull, ps);
+                            if (bal != 0u) {
+                                int base = 0;
+                                if (lane == 0) base = atomicAdd(&qcnt[0], __popc(bal));
+                                base = __shfl_sync(kFull, base, 0);
+                                if (ps) {
+                                    const int d = base + __popc(bal & lt);
+                                    cs[d] = sv;
+                                    ci[d] = pool_g;
+                                }
+                            }
+                        }
+                        PT_MARK(4);
+                        if ((m % Gq) == Gq - 1 && m != nquad - 1) {
+                            ptx::named_bar_sync(1, kEpiThreads);
+                            if (qcnt[0] > room_q) {
+                                if (g == 0) {
+                                    const int nn = group_select(cs, ci, qcnt[0], Kp, false, slack, 0,
+                                                                gtid, hist, gs, &thr_s[0]);
+                                    if (gtid == 0) qcnt[0] = nn;
+                                }
+                                ptx::named_bar_sync(1, kEpiThreads);
+                                thr0 = thr_s[0];
+                            }
+                            PT_MARK(5);
+                        }
+                    }
+                } else {
+                    tiles();
+                }
+            } else {
+                tiles();
+            }
             if (aborted) break;
             if (p.mode == 1) {
                 ptx::named_bar_sync(1, kEpiThreads);   // w staging is rewritten next
@@ -906,7 +1179,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // final selection, pool order and output: every group on its own queries
             PT_MARK(1);
             ptx::named_bar_sync(1, kEpiThreads);
-            for (int q = g; q < nq; q += kGroups) {
+            bool emit = true;
+            if constexpr (kFew) {
+                if (ti_slots[2].splits > 1)
+                    emit = split_unit_end(ti_slots + 2, nq, QT, Kp, C, cs, ci, qcnt, thr_s, hist, gs,
+                                          g, gtid, etid, misc + 2, p.part_idx, p.part_score,
+                                          p.part_cnt, p.tile_ctr);
+            }
+            for (int q = g; q < nq && emit; q += kGroups) {
                 int n = qcnt[q];
                 float *csq = cs + q * C;
                 int *ciq = ci + q * C;
@@ -917,7 +1197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t row = static_cast<int64_t>(t.t0 + q) * Kp;
                 const int nc_q = min((tau0 + q + 1) / p.kp, t.pool_count);   // visible local pools
                 const int words = (nc_q + 31) / 32;
-                if (words <= C - n) {
+                if (words <= (kQuad && nq == 1 ? QT * C : C) - n) {
                     group_rank_store(csq, ciq, n, t.pool_base, words, g, gtid, gs,
                                      p.pool_idx + row, p.pool_score + row);
                 } else {
@@ -1005,6 +1285,129 @@ __global__ void schedule_kernel(const int32_t *cu, int n_docs, int T, int QT, in
     }
 }
 
+// Sum over the block (1024 threads); every thread gets the total.
+__device__ int block_sum(int v, int *red)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    v = __reduce_add_sync(kFull, v);
+    __syncthreads();   // red reuse
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    int tot = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += red[w];
+    return tot;
+}
+
+// Exclusive prefix over the block in thread order; *total gets the sum.
+__device__ int block_exclusive_scan(int v, int *red, int *total)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    __syncthreads();   // red reuse
+    if (lane == 31) red[wid] = incl;
+    __syncthreads();
+    int before = 0, tot = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+        if (w < wid) before += red[w];
+        tot += red[w];
+    }
+    *total = tot;
+    return before + incl - v;
+}
+
+// Split-pool schedule (one block of 1024 threads, one query tile per thread).
+// The W pool tiles of all query tiles are cut into units of about
+// W / (4 * grid) pool tiles (at least kSplitMinTiles): a query tile with more
+// pool tiles becomes min(splits_max, ceil(npt / U)) units of nearly equal
+// length, U doubling until the split units fit the `slots` partial lists.
+// Table: the split units first (tile by tile; their table positions are their
+// partial-list slots), then the unsplit query tiles.  Also validates
+// cu_seqlens and resets the tile counter, the status word and the per-tile
+// arrival counters.
+__global__ void __launch_bounds__(1024)
+    split_schedule_kernel(const int32_t *cu, const int32_t *q_pos, const int32_t *cu_pools,
+                          int n_docs, int T, int P_total, int QT, int kp, int grid, int slots,
+                          int splits_max, int *ws, int *units, int *ctr)
+{
+    __shared__ int s_nt;
+    __shared__ int red[32];
+    if (threadIdx.x == 0) {
+        int ok = 1, nt = 0;
+        if (cu != nullptr) {
+            if (cu[0] != 0 || cu[n_docs] != T) ok = 0;
+            for (int d = 0; d < n_docs && ok; ++d) {
+                const int L = cu[d + 1] - cu[d];
+                if (L < 0) ok = 0;
+                else nt += (L + QT - 1) / QT;
+            }
+        } else {
+            nt = (T + QT - 1) / QT;
+        }
+        if (nt > static_cast<int>(blockDim.x)) ok = 0;
+        s_nt = ok ? nt : 0;
+        ws[WS_COUNTER] = 0;
+        ws[WS_STATUS] = ok ? 0 : KPOOL_STATUS_BAD_SEQLENS;
+    }
+    __syncthreads();
+    const int nt = s_nt;
+    const int g = threadIdx.x;
+    int t0 = 0, d = 0, npt = 0;
+    if (g < nt) {
+        int i = g;
+        if (cu != nullptr) {
+            int acc = 0;
+            for (d = 0; d < n_docs; ++d) {
+                const int n = (cu[d + 1] - cu[d] + QT - 1) / QT;
+                if (g < acc + n) break;
+                acc += n;
+            }
+            i = g - acc;
+        }
+        const int doc_start = cu != nullptr ? cu[d] : 0;
+        const int doc_end = cu != nullptr ? cu[d + 1] : T;
+        const int pool_count = cu != nullptr ? cu_pools[d + 1] - cu_pools[d] : P_total;
+        const int pos = (q_pos != nullptr ? q_pos[d] : 0) + i * QT;
+        t0 = doc_start + i * QT;
+        const int nq = min(QT, doc_end - t0);
+        const int nc_last = min((pos + nq) / kp, pool_count);   // as pool_tiles_of
+        npt = (nc_last + kBM - 1) / kBM;
+    }
+    const int W = block_sum(min(npt, 1 << 20), red);
+    int U = max(kSplitMinTiles, (W + 4 * grid - 1) / (4 * grid));
+    int sp = 1;
+    for (int iter = 0; iter < 31; ++iter) {
+        sp = npt > U ? min(splits_max, (npt + U - 1) / U) : 1;
+        if (block_sum(sp > 1 ? sp : 0, red) <= slots) break;
+        U *= 2;
+    }
+    if (block_sum(sp > 1 ? sp : 0, red) > slots) sp = 1;   // (not reached: U outgrows every npt)
+    int n_split = 0, n_whole = 0;
+    const int ex_s = block_exclusive_scan(sp > 1 ? sp : 0, red, &n_split);
+    const int ex_w = block_exclusive_scan(g < nt && sp == 1 ? 1 : 0, red, &n_whole);
+    int4 *u4 = reinterpret_cast<int4 *>(units);
+    if (g < nt) {
+        ctr[g] = 0;
+        if (sp > 1) {
+            for (int k = 0; k < sp; ++k) {
+                const int at = ex_s + k;
+                u4[2 * at] = make_int4(t0, d, static_cast<int>(static_cast<int64_t>(k) * npt / sp),
+                                       static_cast<int>(static_cast<int64_t>(k + 1) * npt / sp));
+                u4[2 * at + 1] = make_int4(ex_s, sp, g, k);
+            }
+        } else {
+            const int at = n_split + ex_w;
+            u4[2 * at] = make_int4(t0, d, 0, npt);
+            u4[2 * at + 1] = make_int4(-1, 1, g, 0);
+        }
+    }
+    if (threadIdx.x == 0) ws[WS_NTILES] = n_split + n_whole;
+}
+
 __global__ void fill_kernel(uint32_t *a, int64_t n, uint32_t va, uint32_t *b, uint32_t vb)
 {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
@@ -1054,17 +1457,25 @@ int encode_2d(CUtensorMap *m, const void *base, int fp8, uint64_t cols, uint64_t
     return KPOOL_OK;
 }
 
+template <int H, bool kFew>
+int launch_hf(const Layout &L, const CUtensorMap &mq, const CUtensorMap &mpk, const Params &prm,
+              int grid, cudaStream_t s)
+{
+    const int smem = static_cast<int>(L.total) + 1024;
+    KPOOL_CUDA_CHECK(cudaFuncSetAttribute(score_kernel<H, kFew>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    score_kernel<H, kFew><<<grid, kThreads, smem, s>>>(mq, mpk, prm);
+    KPOOL_CUDA_CHECK(cudaGetLastError());
+    return KPOOL_OK;
+}
+
 template <int H>
 int launch_h(const ScoreArgs &a, const Layout &L, const CUtensorMap &mq, const CUtensorMap &mpk,
              const Params &prm, int grid, cudaStream_t s)
 {
-    const int smem = static_cast<int>(L.total) + 1024;
-    KPOOL_CUDA_CHECK(cudaFuncSetAttribute(score_kernel<H>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    score_kernel<H><<<grid, kThreads, smem, s>>>(mq, mpk, prm);
-    KPOOL_CUDA_CHECK(cudaGetLastError());
     (void)a;
-    return KPOOL_OK;
+    return prm.units != nullptr ? launch_hf<H, true>(L, mq, mpk, prm, grid, s)
+                                : launch_hf<H, false>(L, mq, mpk, prm, grid, s);
 }
 
 // Scratch of the allocation-free entry point (kpool_score_topk_noalloc): the
@@ -1120,6 +1531,47 @@ size_t score_workspace_bytes(int64_t T, int H, int n_docs)
     const int64_t max_tiles = (T + QT - 1) / QT + n_docs;
     size_t b = WS_TABLE_INTS * 4 + static_cast<size_t>(max_tiles) * 8;
     return (b + 255) & ~static_cast<size_t>(255);
+}
+
+namespace {
+
+// Workspace layout of the split-pool schedule (offsets in ints from the
+// workspace base), after the header and the one-unit-per-tile table.
+struct SplitLayout {
+    int ok;               // the call may use the split-pool schedule
+    int slots;            // partial lists (split units) per call, at most
+    int max_units;
+    int64_t units_off, ctr_off, cnt_off, idx_off, score_off;
+    size_t bytes;
+};
+
+SplitLayout split_layout(int64_t T, int H, int n_docs, int Kp)
+{
+    SplitLayout s{};
+    const int64_t QT = qt_of(H);
+    const int64_t max_tiles = (T + QT - 1) / QT + n_docs;
+    const size_t base = score_workspace_bytes(T, H, n_docs);
+    s.bytes = base;
+    if (Kp <= 0 || max_tiles > kSplitMaxQT) return s;
+    s.slots = static_cast<int>(std::max<int64_t>(1, kSplitEntries / (QT * Kp)));
+    s.max_units = kSplitMaxQT + s.slots;
+    int64_t off = static_cast<int64_t>(base / 4);
+    s.units_off = off; off += static_cast<int64_t>(s.max_units) * 8;
+    s.ctr_off = off;   off += kSplitMaxQT;
+    s.cnt_off = off;   off += static_cast<int64_t>(s.slots) * QT;
+    off = (off + 63) & ~static_cast<int64_t>(63);
+    s.idx_off = off;   off += static_cast<int64_t>(s.slots) * QT * Kp;
+    s.score_off = off; off += static_cast<int64_t>(s.slots) * QT * Kp;
+    s.bytes = (static_cast<size_t>(off) * 4 + 255) & ~static_cast<size_t>(255);
+    s.ok = 1;
+    return s;
+}
+
+}  // namespace
+
+size_t score_workspace_split_bytes(int64_t T, int H, int n_docs, int Kp)
+{
+    return split_layout(T, H, n_docs, Kp).bytes;
 }
 
 int score_capacity(int H, int D, int fp8)
@@ -1188,10 +1640,29 @@ int run_score(const ScoreArgs &a, cudaStream_t s)
     prm.idesc = ptx::make_idesc(a.fp8 ? 0u : 1u, kBM, kBN);
     prm.L = L;
 
-    schedule_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.n_docs, static_cast<int>(a.T), QT,
-                                       static_cast<int>(max_tiles), a.ws);
+    // few query tiles (decode, short chunks) with room in the workspace: split
+    // their pool lists over the CTAs; C >= 2 Kp lets a merge append a whole
+    // partial list after at most one compaction
+    const SplitLayout SL = split_layout(a.T, a.H, a.n_docs, a.Kp);
+    const bool split = a.mode == 0 && SL.ok && a.ws_bytes >= SL.bytes && L.C >= 2 * a.Kp;
+    int grid;
+    if (split) {
+        prm.units = a.ws + SL.units_off;
+        prm.tile_ctr = a.ws + SL.ctr_off;
+        prm.part_cnt = a.ws + SL.cnt_off;
+        prm.part_idx = a.ws + SL.idx_off;
+        prm.part_score = reinterpret_cast<float *>(a.ws + SL.score_off);
+        grid = num_sms();
+        split_schedule_kernel<<<1, kSplitMaxQT, 0, s>>>(
+            a.cu_seqlens, a.q_pos, a.cu_pools, a.n_docs, static_cast<int>(a.T),
+            static_cast<int>(a.P_total), QT, a.kpool, grid, SL.slots, kSplitMaxSplits, a.ws,
+            prm.units, prm.tile_ctr);
+    } else {
+        schedule_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.n_docs, static_cast<int>(a.T), QT,
+                                           static_cast<int>(max_tiles), a.ws);
+        grid = static_cast<int>(std::min<int64_t>(num_sms(), max_tiles));
+    }
     KPOOL_CUDA_CHECK(cudaGetLastError());
-    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), max_tiles));
     switch (a.H) {
     case 4: return launch_h<4>(a, L, mq, mpk, prm, grid, s);
     case 8: return launch_h<8>(a, L, mq, mpk, prm, grid, s);

@@ -160,3 +160,73 @@ def test_fullsize_chunk_16k_of_128k(K, ora):
 def test_fullsize_decode_128x32k(K, ora):
     inp, idx = _fullsize(K, ora, "decode_128x32k", 1024)   # 128 rows: all of them
     assert inp.Tq == 128 and np.all(idx >= 0)
+
+
+def _split_vs_unsplit(K, ora, wl, n_check):
+    """kpool_score_topk_at with a workspace that enables the split-pool
+    schedule against the same call with the minimal workspace (one unit per
+    query tile): identical outputs, bit for bit; plus oracle rows."""
+    dev = torch.device("cuda")
+    inp = W.make_inputs(wl)
+    cu_k = inp.cu_seqlens.numpy()
+    n_docs = len(cu_k) - 1
+    cu_pools_h, P = K.kpool_num_pools(inp.cu_seqlens, wl.T, wl.kpool)
+    d_ck, d_cp = inp.cu_seqlens.to(dev), cu_pools_h.to(dev)
+    pk = K.kpool_compress(inp.k.to(dev), inp.gate.to(dev), inp.ape.to(dev), wl.kpool, d_ck, d_cp,
+                          P)
+    d_cq, d_qp = inp.cu_q.to(dev), inp.q_pos.to(dev)
+    q, w = inp.q.to(dev), inp.w.to(dev)
+    Tq, H = inp.Tq, wl.H
+    ws_split = K.new_workspace(Tq, H, n_docs, dev, wl.kpool, wl.index_topk)
+    ws_one = K.new_workspace(Tq, H, n_docs, dev)
+    assert ws_split.numel() > ws_one.numel()
+    a = K.kpool_score_topk_at(q, w, pk, wl.kpool, wl.index_topk, d_cq, d_qp, d_cp,
+                              workspace=ws_split)
+    b = K.kpool_score_topk_at(q, w, pk, wl.kpool, wl.index_topk, d_cq, d_qp, d_cp,
+                              workspace=ws_one)
+    torch.cuda.synchronize()
+    assert K.kpool_read_status(ws_split) == 0 and K.kpool_read_status(ws_one) == 0
+    assert torch.equal(a[0], b[0])
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+    from kpool_checks import bf16_bits
+    pkb = bf16_bits(pk)
+    cq, qp = inp.cu_q.numpy(), inp.q_pos.numpy()
+    rows = np.unique(np.linspace(0, Tq - 1, n_check).astype(np.int64))
+    ops = ora.Operands(W.bits(inp.q), inp.w.numpy(), pkb)
+
+    class At:
+        select_rows = staticmethod(lambda ops_, cu, kp, Kp, r: ora.select_rows_at(
+            ops_, cq, qp, cu_k, kp, Kp, r))
+        score_pairs = staticmethod(lambda ops_, cu, kp, r, p: ora.score_pairs_at(
+            ops_, cq, qp, cu_k, kp, r, p))
+    idx, sc = a[0].cpu().numpy(), a[1].cpu().numpy()
+    check_selection(At, ops, None, wl.kpool, wl.Kp, rows, idx[rows], sc[rows], TOL, wl.name)
+    return idx
+
+
+def test_split_schedule_decode_long_documents(K, ora):
+    """48 decode queries over documents of 2K-30K keys: pool lists of up to 60
+    tiles, cut into up to 16 units each."""
+    wl = W.Workload("split_decode", T=48 * 16384, H=64, D=128, kpool=4, index_topk=2048,
+                    n_docs=48, doc_len_range=(2048, 30720), queries="last", seed=21)
+    idx = _split_vs_unsplit(K, ora, wl, 12)
+    assert np.all(idx >= 0)
+
+
+def test_split_schedule_chunks_share_units(K, ora):
+    """Chunks of 37 queries (full and ragged query tiles) at the end of two
+    long documents: every query of a split tile is merged."""
+    wl = W.Workload("split_chunk", T=2 * 20000, H=64, D=128, kpool=4, index_topk=512,
+                    n_docs=2, equal_docs=True, queries="chunk:37", seed=22)
+    _split_vs_unsplit(K, ora, wl, 16)
+
+
+def test_split_schedule_small_heads_and_large_budget(K, ora):
+    """H = 16 (16 queries per tile) with Kp = 256, and kpool = 2 with Kp = 1024
+    (too large to merge in place: the call runs unsplit)."""
+    wl = W.Workload("split_h16", T=8 * 6000, H=16, D=64, kpool=4, index_topk=1024,
+                    n_docs=8, equal_docs=True, queries="chunk:21", seed=23)
+    _split_vs_unsplit(K, ora, wl, 16)
+    wl = W.Workload("split_kp2", T=4 * 12000, H=64, D=128, kpool=2, index_topk=2048,
+                    n_docs=4, equal_docs=True, queries="last", seed=24)
+    _split_vs_unsplit(K, ora, wl, 4)
