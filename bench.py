@@ -386,20 +386,25 @@ def main():
             raise B.KPoolError(rc, name)
 
     def step(ev=None):
+        # segments: compress | quantize q (FP8 mode; empty otherwise) | score | expand
         if ev is not None:
             ev[0].record(stream)
         if wl.fp8:
             chk(L.kpool_compress(B._ptr(k), B._ptr(gate), B._ptr(ape), B._ptr(cu), B._ptr(cp),
                                  n_docs, T, D, kp, P, B._ptr(pk), B._ptr(pk8), B._ptr(pks), sp),
                 "kpool_compress")
+            if ev is not None:
+                ev[1].record(stream)
             chk(L.kpool_quantize_fp8(B._ptr(q), T * H, D, B._ptr(q8), B._ptr(qs), sp),
                 "kpool_quantize_fp8")
         else:
             chk(L.kpool_compress(B._ptr(k), B._ptr(gate), B._ptr(ape), B._ptr(cu), B._ptr(cp),
                                  n_docs, T, D, kp, P, B._ptr(pk), None, None, sp),
                 "kpool_compress")
+            if ev is not None:
+                ev[1].record(stream)
         if ev is not None:
-            ev[1].record(stream)
+            ev[2].record(stream)
         if wl.fp8:
             chk(L.kpool_score_topk(B._ptr(q8), B._ptr(qs), B._ptr(w), B._ptr(pk8), B._ptr(pks),
                                    B._ptr(cu), B._ptr(cp), n_docs, T, P, H, D, kp, topk, 1,
@@ -411,11 +416,11 @@ def main():
                                    B._ptr(pool_score), B._ptr(ws), ws.numel(), sp),
                 "kpool_score_topk")
         if ev is not None:
-            ev[2].record(stream)
+            ev[3].record(stream)
         chk(L.kpool_expand_indices(B._ptr(pool_idx), B._ptr(cu), B._ptr(cp), n_docs, T, kp, topk,
                                    int(wl.tail), B._ptr(tok), sp), "kpool_expand_indices")
         if ev is not None:
-            ev[3].record(stream)
+            ev[4].record(stream)
 
     launches_per_step = 1 + (1 if wl.fp8 else 0) + 2 + 1
 
@@ -431,8 +436,8 @@ def main():
         raise RuntimeError("device status %d after warm-up" % status)
 
     in_bytes = sum(x.numel() * x.element_size() for x in (q, k, gate, w))
-    ms_step, (t_compress, t_score, t_expand), clocks, l2_note = timed_loop(
-        step, 3, args.steps, stream, in_bytes, local, barrier)
+    ms_step, (t_compress, t_quant, t_score, t_expand), clocks, l2_note = timed_loop(
+        step, 4, args.steps, stream, in_bytes, local, barrier)
     ms_step = job_time_ms(ms_step, world, dev)
     status = K.kpool_read_status(ws)
     if status != 0:
@@ -492,9 +497,12 @@ def main():
                 "frac_of_burst": achieved / (peaks["bf16_tflops"] * (2 if wl.fp8 else 1)),
                 "algorithmic_flops_per_launch": flops, "causal_pairs": pairs,
                 "ms_per_launch": t_score}
-    comp_bytes = T * D * 2 * 2 + P * D * 2
+    comp_bytes = T * D * 2 * 2 + P * D * 2 + (P * (D + 4) if wl.fp8 else 0)
     side = {"compress_ms": t_compress, "compress_gbs": comp_bytes / (t_compress / 1000.0) / 1e9,
             "compress_frac_hbm": comp_bytes / (t_compress / 1000.0) / 1e9 / peaks["hbm_gbs"],
+            "quantize_q_ms": t_quant if wl.fp8 else None,
+            "quantize_q_gbs": (T * H * (D * 2 + D + 4)) / (t_quant / 1000.0) / 1e9
+            if wl.fp8 else None,
             "expand_ms": t_expand,
             "expand_gbs": (T * Kp * 4 + T * Wd * 4) / (t_expand / 1000.0) / 1e9,
             "score_topk_ms": t_score, "score_queries_per_s": T / (t_score / 1000.0)}

@@ -233,22 +233,100 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(
     }
 }
 
+// The same chain for rows handled by 8 threads of 16 elements (slice v of the
+// row): butterflies over element-index bits 0-3 in the thread, bits 4-6 across
+// threads, in the same stage order as fp8_row, so the results are identical.
+__device__ __forceinline__ void fp8_row16(float (&x)[16], int v, uint8_t *codes16,
+                                          float *scale_out, bool active)
+{
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float o = __shfl_xor_sync(0xFFFFFFFFu, x[i], m);
+            x[i] = (v & m) ? (o - x[i]) : (x[i] + o);
+        }
+    }
+    const float norm = 0.08838834764831845f;   // 128^-1/2
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = __uint_as_float(bf16_bits_rn(x[i] * norm) << 16);
+        amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    int e = 0;
+    if (amax > 0.f) {
+        int E;
+        const float f = frexpf(amax, &E);
+        e = E - 9 + (f > 0.875f ? 1 : 0);
+    }
+    const float s = ldexpf(1.f, e);
+    if (!active) return;
+    const bool mul_ok = e > -126 && e < 126;
+    const float inv = mul_ok ? ldexpf(1.f, -e) : 1.f;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float y0 = mul_ok ? x[i] * inv : ldexpf(x[i], -e);
+        const float y1 = mul_ok ? x[i + 1] * inv : ldexpf(x[i + 1], -e);
+        // element i in the low byte, i + 1 in the high byte
+        const uint32_t c2 = static_cast<uint32_t>(
+            __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3));
+        w[i >> 2] |= c2 << (8 * (i & 3));
+    }
+    *reinterpret_cast<uint4 *>(codes16) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (v == 0) *scale_out = s;
+}
+
+// q rows: 8 threads per row; a warp covers 8 consecutive rows, each thread two
+// of them (rows 4 apart), with all four 16-byte loads issued before any math.
+constexpr int kQuantRowsPerWarp = 8;
+
 __global__ void __launch_bounds__(kThreads) quantize_fp8_kernel(
     const uint16_t *__restrict__ x, int64_t rows, uint8_t *__restrict__ out,
     float *__restrict__ scale)
 {
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    const int64_t r = gid >> 4;
-    const int v = static_cast<int>(gid & 15);
-    const bool active = r < rows;
-    float f[8];
-    if (active) {
-        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(x + r * 128 + v * 8), f);
-    } else {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int v = lane & 7;
+    int64_t r[2];
+    bool act[2];
+    uint4 raw[2][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    for (int k = 0; k < 2; ++k) {
+        r[k] = warp * kQuantRowsPerWarp + 4 * k + (lane >> 3);
+        act[k] = r[k] < rows;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (act[k] ? r[k] : 0) * 128 + v * 16);
+        raw[k][0] = act[k] ? src[0] : make_uint4(0u, 0u, 0u, 0u);
+        raw[k][1] = act[k] ? src[1] : make_uint4(0u, 0u, 0u, 0u);
     }
-    fp8_row(f, v, out + (active ? r : 0) * 128 + v * 8, scale + (active ? r : 0), active);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float f[16];
+        float lo[8], hi[8];
+        bf16x8_to_f32(raw[k][0], lo);
+        bf16x8_to_f32(raw[k][1], hi);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            f[i] = lo[i];
+            f[8 + i] = hi[i];
+        }
+        fp8_row16(f, v, out + (act[k] ? r[k] : 0) * 128 + v * 16, scale + (act[k] ? r[k] : 0),
+                  act[k]);
+    }
 }
 
 __global__ void cu_pools_kernel(const int32_t *cu_seqlens, int n_docs, int kp, int32_t *cu_pools)
@@ -299,7 +377,8 @@ cudaError_t launch_quantize_fp8(const void *x, int64_t rows, uint8_t *out, float
                                 cudaStream_t s)
 {
     if (rows == 0) return cudaSuccess;
-    const int64_t blocks = (rows * 16 + kThreads - 1) / kThreads;
+    const int64_t warps = (rows + kQuantRowsPerWarp - 1) / kQuantRowsPerWarp;
+    const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
     quantize_fp8_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
         static_cast<const uint16_t *>(x), rows, out, scale);
     return cudaGetLastError();

@@ -8,6 +8,7 @@ of cycles in each phase, summed over all CTAs.
 
     python -m sparse_attention_kpool_compress_gb300.phase_report [T ...]
     python -m sparse_attention_kpool_compress_gb300.phase_report decode:B:LO:HI
+    python -m sparse_attention_kpool_compress_gb300.phase_report fp8:T
 
 ``decode:B:LO:HI`` runs ``kpool_score_topk_at`` on B documents with seeded
 key lengths uniform in [LO, HI) and one query each at its last key, with a
@@ -100,7 +101,8 @@ def run_decode(B_docs: int, lo: int, hi: int, H: int = 64, D: int = 128, kpool: 
     return _report(lib, call, res)
 
 
-def run(T: int, H: int = 64, D: int = 128, kpool: int = 4, index_topk: int = 2048, seed: int = 0):
+def run(T: int, H: int = 64, D: int = 128, kpool: int = 4, index_topk: int = 2048, seed: int = 0,
+        fp8: bool = False):
     lib = ctypes.CDLL(B.build(variant="phase_timers"))
     P = ctypes.c_void_p
     lib.kpool_score_topk_workspace_size.restype = ctypes.c_size_t
@@ -113,6 +115,19 @@ def run(T: int, H: int = 64, D: int = 128, kpool: int = 4, index_topk: int = 204
     q = torch.randn(T, H, D, device="cuda", generator=g).to(torch.bfloat16)
     pk = torch.randn(T // kpool, D, device="cuda", generator=g).to(torch.bfloat16)
     w = torch.randn(T, H, device="cuda", generator=g) / H ** 0.5
+    qs = pks = None
+    if fp8:
+        lib.kpool_quantize_fp8.argtypes = [P, ctypes.c_int64, ctypes.c_int, P, P, P]
+        q8 = torch.empty(T, H, D, dtype=torch.uint8, device="cuda")
+        qs = torch.empty(T, H, dtype=torch.float32, device="cuda")
+        pk8 = torch.empty(T // kpool, D, dtype=torch.uint8, device="cuda")
+        pks = torch.empty(T // kpool, dtype=torch.float32, device="cuda")
+        for src, dst, sc, rows in ((q, q8, qs, T * H), (pk, pk8, pks, T // kpool)):
+            if lib.kpool_quantize_fp8(ctypes.c_void_p(src.data_ptr()), rows, D,
+                                      ctypes.c_void_p(dst.data_ptr()),
+                                      ctypes.c_void_p(sc.data_ptr()), None) != 0:
+                raise RuntimeError("kpool_quantize_fp8 failed")
+        q, pk = q8, pk8
     Kp = index_topk // kpool
     idx = torch.empty(T, Kp, dtype=torch.int32, device="cuda")
     sc = torch.empty(T, Kp, dtype=torch.float32, device="cuda")
@@ -121,9 +136,10 @@ def run(T: int, H: int = 64, D: int = 128, kpool: int = 4, index_topk: int = 204
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())
 
     def call():
-        rc = lib.kpool_score_topk(ptr(q), None, ptr(w), ptr(pk), None, None, None, 1, T,
-                                  T // kpool, H, D, kpool, index_topk, 0, ptr(idx), ptr(sc),
-                                  ptr(ws), nws, None)
+        rc = lib.kpool_score_topk(ptr(q), ptr(qs) if fp8 else None, ptr(w), ptr(pk),
+                                  ptr(pks) if fp8 else None, None, None, 1, T, T // kpool, H, D,
+                                  kpool, index_topk, int(fp8), ptr(idx), ptr(sc), ptr(ws), nws,
+                                  None)
         if rc != 0:
             raise RuntimeError(lib.kpool_last_error())
 
@@ -138,7 +154,7 @@ def run(T: int, H: int = 64, D: int = 128, kpool: int = 4, index_topk: int = 204
     torch.cuda.synchronize()
     lib.kpool_debug_phase_timers(out, 1)
     v = list(out)
-    res = {"T": T, "H": H, "D": D, "kpool": kpool, "index_topk": index_topk,
+    res = {"T": T, "H": H, "D": D, "kpool": kpool, "index_topk": index_topk, "fp8": fp8,
            "ms": e0.elapsed_time(e1)}
     for key, base, names in (("epilogue", 24, EPI), ("mma", 8, MMA), ("producer", 16, PROD)):
         tot = sum(v[base:base + 8]) or 1
@@ -148,7 +164,9 @@ def run(T: int, H: int = 64, D: int = 128, kpool: int = 4, index_topk: int = 204
 
 if __name__ == "__main__":
     for arg in sys.argv[1:] or ["131072"]:
-        if arg.startswith("decode:"):
+        if arg.startswith("fp8:"):
+            print(json.dumps(run(int(arg.split(":")[1]), fp8=True)))
+        elif arg.startswith("decode:"):
             _, b, lo, hi = arg.split(":")
             print(json.dumps(run_decode(int(b), int(lo), int(hi))))
         else:

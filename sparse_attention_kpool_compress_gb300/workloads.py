@@ -72,6 +72,9 @@ WORKLOADS = {
                           n_docs=2, equal_docs=True, fp8=True,
                           desc="FP8 indexer mode: 2 sequences of 32768 tokens, H=64 D=128 "
                                "kpool=4 index_topk=2048, E4M3 scoring"),
+    "fp8_128k": Workload("fp8_128k", T=131072, H=64, D=128, kpool=4, index_topk=2048, fp8=True,
+                         desc="FP8 indexer mode at T=131072: one sequence, H=64 D=128 kpool=4 "
+                              "index_topk=2048, E4M3 scoring"),
     "chunk_16k_of_128k": Workload("chunk_16k_of_128k", T=131072, H=64, D=128, kpool=4,
                                   index_topk=2048, queries="chunk:16384",
                                   desc="Chunked prefill: the last 16384-token chunk of a "

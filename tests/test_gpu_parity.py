@@ -130,6 +130,24 @@ def test_quantize_fp8_matches_oracle(K, ora):
     assert float(sc[5]) == 1.0 and int(codes[5].abs().sum()) == 0
 
 
+def test_quantize_fp8_ragged_rows(K):
+    """Row counts that do not fill the last warp: the same codes as the full
+    call, and nothing written past the last row."""
+    gen = torch.Generator().manual_seed(13)
+    x = dev(torch.randn(4096, 128, generator=gen).to(torch.bfloat16))
+    full_c, full_s = K.kpool_quantize_fp8(x)
+    B = K.binding
+    for rows in (4093, 4089, 1):
+        c = torch.full((4096, 128), 0xAB, dtype=torch.uint8, device=x.device)
+        sc = torch.full((4096,), 7.0, dtype=torch.float32, device=x.device)
+        rc = B._lib.kpool_quantize_fp8(B._ptr(x), rows, 128, B._ptr(c), B._ptr(sc),
+                                       B._stream(x.device))
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert torch.equal(c[:rows], full_c[:rows]) and torch.equal(sc[:rows], full_s[:rows])
+        assert bool((c[rows:] == 0xAB).all()) and bool((sc[rows:] == 7.0).all())
+
+
 def test_compress_fp8_matches_oracle(K, ora):
     wl = W.Workload("f", T=4096, H=4, D=128, kpool=4, index_topk=64)
     inp = W.make_inputs(wl, seed=12)
