@@ -292,6 +292,45 @@ KPOOL_API int kpool_expand_indices(const int32_t *pool_idx, const int32_t *cu_se
                          kpool_stream_t stream);
 
 /*
+ * kpool_indexer_forward_host -- the whole indexer pass from HOST buffers to
+ * HOST token indices (Megatron-LM PR section 3: compression, pool top-k,
+ * expansion with the causal tail, packed THD; the FP8 input path), with the
+ * host<->device copies overlapped with the kernels.  Keys are copied and
+ * compressed first; the query rows then go in chunks of chunk_rows (0 =
+ * 16384) over three internal streams: the copy-in of chunk c+1, the scoring
+ * and expansion of chunk c and the copy-out of chunk c-1 run concurrently.
+ * Each chunk is scored as positioned queries over the global pooled keys, so
+ * tok_idx_out equals what kpool_compress -> [kpool_quantize_fp8] ->
+ * kpool_score_topk -> kpool_expand_indices give on the same inputs.
+ *   q      bf16 [T, H, D]      k, gate  bf16 [T, D]     ape  fp32 [kpool, D]
+ *   w      fp32 [T, H]         tok_idx_out  int32 [T, Kp*kpool + kpool - 1]
+ *   cu_seqlens_host  int32 [n_docs + 1] host array (NULL = one sequence,
+ *                    n_docs = 1), validated on the host
+ * All of these are host memory; page-locked (cudaHostAlloc / pinned)
+ * buffers are needed for the copies to overlap, pageable ones work but
+ * serialise.  fp8 = 1 runs the FP8 mode (D = 128).
+ *   scratch  device memory of at least kpool_indexer_forward_host_scratch_size
+ *            bytes, 256-byte aligned, owned by the caller; its first 256 bytes
+ *            carry the pass's status word (kpool_read_status(scratch, ...)).
+ * Asynchronous on `stream`: the call returns once the work is enqueued, and
+ * `stream` waits for the last copy-out; synchronise it before reading
+ * tok_idx_out or reusing the host inputs.  The internal streams and events
+ * belong to the calling host thread (created on its first call per device).
+ * Errors: as kpool_score_topk, plus KPOOL_ERR_WORKSPACE for a short scratch.
+ */
+KPOOL_API size_t kpool_indexer_forward_host_scratch_size(const int32_t *cu_seqlens_host,
+                                                         int n_docs, int64_t T, int H, int D,
+                                                         int kpool, int index_topk, int fp8,
+                                                         int64_t chunk_rows);
+KPOOL_API int kpool_indexer_forward_host(const void *q, const void *k, const void *gate,
+                                         const float *ape, const float *w,
+                                         const int32_t *cu_seqlens_host, int n_docs, int64_t T,
+                                         int H, int D, int kpool, int index_topk,
+                                         int always_select_tail, int fp8, int64_t chunk_rows,
+                                         int32_t *tok_idx_out, void *scratch,
+                                         size_t scratch_bytes, kpool_stream_t stream);
+
+/*
  * kpool_read_status -- debug helper: synchronously copy the device status
  * word of a workspace (KPOOL_STATUS_* bits, 0 = clean) to *status_out.
  * Synchronises the whole device.

@@ -55,6 +55,9 @@ _SIGS = {
                                  _P, _P, _P, _SZ, _P]),
     "kpool_expand_indices_at": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _P, _P]),
     "kpool_read_status": (_I, [_P, _P]),
+    "kpool_indexer_forward_host_scratch_size": (_SZ, [_P, _I, _L, _I, _I, _I, _I, _I, _L]),
+    "kpool_indexer_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _I, _I, _I,
+                                        _L, _P, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -321,6 +324,55 @@ def kpool_expand_indices_at(pool_idx, kpool: int, index_topk: int, cu_seqlens_q,
                                         _ptr(tok), _stream(pool_idx.device)),
            "kpool_expand_indices_at")
     return tok
+
+
+def _host_cu(cu_seqlens_host):
+    if cu_seqlens_host is None:
+        return None, 1
+    _need(cu_seqlens_host, "cu_seqlens_host", torch.int32, device=False)
+    if cu_seqlens_host.is_cuda:
+        raise ValueError("cu_seqlens_host must be a CPU tensor")
+    return cu_seqlens_host, cu_seqlens_host.numel() - 1
+
+
+def kpool_indexer_forward_host_scratch_size(T: int, H: int, D: int, kpool: int, index_topk: int,
+                                            cu_seqlens_host=None, fp8: bool = False,
+                                            chunk_rows: int = 0) -> int:
+    cu, n_docs = _host_cu(cu_seqlens_host)
+    return int(_lib.kpool_indexer_forward_host_scratch_size(_ptr(cu), n_docs, T, H, D, kpool,
+                                                            index_topk, int(fp8), chunk_rows))
+
+
+def kpool_indexer_forward_host(q, k, gate, ape, w, kpool: int, index_topk: int,
+                               always_select_tail: bool = True, cu_seqlens_host=None,
+                               fp8: bool = False, chunk_rows: int = 0, scratch=None, out=None,
+                               device=None):
+    """The whole pass from host (CPU, ideally pinned) tensors to host token
+    indices int32 [T, Kp*kpool + kpool - 1], copies overlapped with the
+    kernels.  Enqueued on the current CUDA stream of `device`; synchronize it
+    before reading the result."""
+    for t_, n_, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16),
+                       (gate, "gate", torch.bfloat16), (ape, "ape", torch.float32),
+                       (w, "w", torch.float32)):
+        _need(t_, n_, dt, device=False)
+        if t_.is_cuda:
+            raise ValueError("%s must be a host tensor" % n_)
+    cu, n_docs = _host_cu(cu_seqlens_host)
+    T, H, D = q.shape
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    W = (index_topk // kpool) * kpool + kpool - 1
+    if out is None:
+        out = torch.empty(T, W, dtype=torch.int32, pin_memory=True)
+    if scratch is None:
+        n = kpool_indexer_forward_host_scratch_size(T, H, D, kpool, index_topk, cu, fp8,
+                                                    chunk_rows)
+        scratch = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    _check(_lib.kpool_indexer_forward_host(_ptr(q), _ptr(k), _ptr(gate), _ptr(ape), _ptr(w),
+                                           _ptr(cu), n_docs, T, H, D, kpool, index_topk,
+                                           int(bool(always_select_tail)), int(fp8), chunk_rows,
+                                           _ptr(out), _ptr(scratch), scratch.numel(),
+                                           _stream(dev)), "kpool_indexer_forward_host")
+    return out
 
 
 def kpool_read_status(workspace) -> int:

@@ -408,6 +408,109 @@ int kpool_expand_indices(const int32_t *pool_idx, const int32_t *cu_seqlens,
     return KPOOL_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Host-side layout check of a host cu_seqlens; fills *P_total.
+int host_layout(const int32_t *cu_host, int n_docs, int64_t T, int kpool, int64_t *P_total)
+{
+    if (!cu_host) {
+        *P_total = T / kpool;
+        return KPOOL_OK;
+    }
+    if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1 (got %d)", n_docs);
+    if (cu_host[0] != 0 || cu_host[n_docs] != T)
+        return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens must run from 0 to T");
+    int64_t P = 0;
+    for (int d = 0; d < n_docs; ++d) {
+        const int64_t L = static_cast<int64_t>(cu_host[d + 1]) - cu_host[d];
+        if (L < 0) return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens must be non-decreasing");
+        P += L / kpool;
+    }
+    *P_total = P;
+    return KPOOL_OK;
+}
+
+int check_forward_shapes(int64_t T, int H, int D, int kpool, int index_topk, int fp8)
+{
+    int rc = check_common(T, kpool);
+    if (rc) return rc;
+    if ((rc = check_h(H))) return rc;
+    if (fp8 ? D != 128 : (D != 32 && D != 64 && D != 128))
+        return fail(KPOOL_ERR_UNSUPPORTED, "D must be 32, 64 or 128 (128 in FP8 mode)");
+    if (index_topk < 1 || index_topk % kpool != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
+    const int Kp = index_topk / kpool;
+    const int cap = score_capacity(H, D, fp8);
+    int kp2 = 1;
+    while (kp2 < Kp) kp2 <<= 1;
+    if (Kp + 128 > cap || kp2 > cap)
+        return fail(KPOOL_ERR_UNSUPPORTED,
+                    "index_topk / kpool = %d exceeds the per-query candidate capacity %d", Kp,
+                    cap);
+    if (T * H > 0x7FFFFFFFLL) return fail(KPOOL_ERR_UNSUPPORTED, "T * H exceeds 2^31 - 1");
+    return KPOOL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kpool_indexer_forward_host_scratch_size(const int32_t *cu_seqlens_host, int n_docs,
+                                               int64_t T, int H, int D, int kpool,
+                                               int index_topk, int fp8, int64_t chunk_rows)
+{
+    if (chunk_rows < 0 || check_forward_shapes(T, H, D, kpool, index_topk, fp8)) return 0;
+    int64_t P = 0;
+    if (host_layout(cu_seqlens_host, cu_seqlens_host ? n_docs : 1, T, kpool, &P)) return 0;
+    return pipeline_scratch_bytes(T, H, D, cu_seqlens_host ? n_docs : 1, kpool, index_topk, fp8,
+                                  chunk_rows, P);
+}
+
+int kpool_indexer_forward_host(const void *q, const void *k, const void *gate, const float *ape,
+                               const float *w, const int32_t *cu_seqlens_host, int n_docs,
+                               int64_t T, int H, int D, int kpool, int index_topk,
+                               int always_select_tail, int fp8, int64_t chunk_rows,
+                               int32_t *tok_idx_out, void *scratch, size_t scratch_bytes,
+                               kpool_stream_t stream)
+{
+    clear_error();
+    int rc = check_forward_shapes(T, H, D, kpool, index_topk, fp8);
+    if (rc) return rc;
+    if (chunk_rows < 0) return fail(KPOOL_ERR_INVALID_ARG, "chunk_rows < 0");
+    if (!cu_seqlens_host) n_docs = 1;
+    int64_t P = 0;
+    if ((rc = host_layout(cu_seqlens_host, n_docs, T, kpool, &P))) return rc;
+    if (T == 0) return KPOOL_OK;
+    if (!q || !k || !gate || !ape || !w || !tok_idx_out)
+        return fail(KPOOL_ERR_INVALID_ARG, "NULL host pointer");
+    if (!scratch) return fail(KPOOL_ERR_WORKSPACE, "scratch is NULL");
+    if (!aligned(scratch, 256))
+        return fail(KPOOL_ERR_INVALID_ARG, "scratch must be 256-byte aligned");
+    PipelineArgs a{};
+    a.q = q;
+    a.k = k;
+    a.gate = gate;
+    a.ape = ape;
+    a.w = w;
+    a.cu_seqlens_host = cu_seqlens_host;   // NULL: one sequence
+    a.n_docs = n_docs;
+    a.T = T;
+    a.P_total = P;
+    a.chunk_rows = chunk_rows;
+    a.H = H;
+    a.D = D;
+    a.kpool = kpool;
+    a.index_topk = index_topk;
+    a.tail = always_select_tail ? 1 : 0;
+    a.fp8 = fp8 ? 1 : 0;
+    a.tok_out = tok_idx_out;
+    a.scratch = scratch;
+    a.scratch_bytes = scratch_bytes;
+    return run_pipeline(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kpool_read_status(const void *workspace, int *status_out)
 {
     clear_error();

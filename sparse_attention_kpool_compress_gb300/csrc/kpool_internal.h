@@ -73,6 +73,24 @@ size_t score_workspace_bytes(int64_t T, int H, int n_docs);
 size_t score_workspace_split_bytes(int64_t T, int H, int n_docs, int Kp);
 int score_capacity(int H, int D, int fp8);   // candidate slots per query (0 = unsupported)
 int run_score(const ScoreArgs &a, cudaStream_t s);
+// Host-buffer pass with copies overlapped (kpool_pipeline.cu).  All input
+// pointers are host memory; cu_seqlens_host NULL means one sequence (n_docs =
+// 1); arguments are validated by the caller.
+struct PipelineArgs {
+    const void *q, *k, *gate;
+    const float *ape, *w;
+    const int32_t *cu_seqlens_host;
+    int n_docs;
+    int64_t T, P_total, chunk_rows;
+    int H, D, kpool, index_topk, tail, fp8;
+    int32_t *tok_out;
+    void *scratch;
+    size_t scratch_bytes;
+};
+size_t pipeline_scratch_bytes(int64_t T, int H, int D, int n_docs, int kpool, int index_topk,
+                              int fp8, int64_t chunk_rows, int64_t P_total);
+int run_pipeline(const PipelineArgs &a, cudaStream_t stream);
+
 // Query tiles the fixed scratch of kpool_score_topk_noalloc can schedule.
 constexpr int kNoAllocMaxTiles = 131072;
 // Device address, size and tile capacity of the no-alloc scratch array of

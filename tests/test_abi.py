@@ -133,3 +133,28 @@ def test_host_validation_rejects_bad_arguments(lib):
         assert rc == code, (fn.__name__, rc, L.kpool_last_error())
         assert L.kpool_last_error()
     del keep
+
+
+def test_host_pipeline_sizes_and_validation():
+    """kpool_indexer_forward_host: scratch size 0 for unsupported shapes,
+    layout errors caught on the host before any device work."""
+    import ctypes
+    import sparse_attention_kpool_compress_gb300 as K
+    assert K.kpool_indexer_forward_host_scratch_size(4096, 64, 128, 4, 2048) > 0
+    assert K.kpool_indexer_forward_host_scratch_size(4096, 7, 128, 4, 2048) == 0      # H
+    assert K.kpool_indexer_forward_host_scratch_size(4096, 64, 96, 4, 2048) == 0      # D
+    assert K.kpool_indexer_forward_host_scratch_size(4096, 64, 64, 4, 2048, fp8=True) == 0
+    assert K.kpool_indexer_forward_host_scratch_size(4096, 64, 128, 4, 2047) == 0     # topk
+    a = K.kpool_indexer_forward_host_scratch_size(4096, 64, 128, 4, 2048, chunk_rows=1024)
+    b = K.kpool_indexer_forward_host_scratch_size(4096, 64, 128, 4, 2048, chunk_rows=2048)
+    assert 0 < a < b
+    L = K.binding._lib
+    bad = (ctypes.c_int32 * 3)(0, 10, 5)          # decreasing offsets
+    dummy = ctypes.c_void_p(16)
+    rc = L.kpool_indexer_forward_host(dummy, dummy, dummy, dummy, dummy,
+                                      ctypes.cast(bad, ctypes.c_void_p), 2, 5, 64, 128, 4, 2048,
+                                      1, 0, 0, dummy, ctypes.c_void_p(256), 1 << 20, None)
+    assert rc == -1                                # KPOOL_ERR_INVALID_ARG
+    rc = L.kpool_indexer_forward_host(dummy, dummy, dummy, dummy, dummy, None, 1, 5, 64, 128, 4,
+                                      2048, 1, 0, -1, dummy, ctypes.c_void_p(256), 1 << 20, None)
+    assert rc == -1                                # negative chunk_rows

@@ -1,0 +1,83 @@
+"""kpool_indexer_forward_host (host buffers in, host token indices out, copies
+overlapped with the kernels over query chunks) against the device path
+kpool_indexer_forward on the same inputs: identical token indices, bit for
+bit, for chunk sizes that cut through query tiles and documents."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_kpool_compress_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_attention_kpool_compress_gb300 as K
+    return K
+
+
+def _device_tokens(K, inp, wl, fp8):
+    dev = torch.device("cuda")
+    cu = inp.cu_seqlens
+    multi = cu.numel() > 2
+    cu_d = cp_d = P = None
+    if multi:
+        cp_h, P = K.kpool_num_pools(cu, wl.T, wl.kpool)
+        cu_d, cp_d = cu.to(dev), cp_h.to(dev)
+    tok, _, _ = K.kpool_indexer_forward(inp.q.to(dev), inp.k.to(dev), inp.gate.to(dev),
+                                        inp.ape.to(dev), inp.w.to(dev), wl.kpool, wl.index_topk,
+                                        wl.tail, cu_d, cp_d, P, fp8=fp8)
+    torch.cuda.synchronize()
+    return tok.cpu()
+
+
+def _host_tokens(K, inp, wl, fp8, chunk_rows):
+    pin = lambda x: x.contiguous().pin_memory()   # noqa: E731
+    cu = inp.cu_seqlens if inp.cu_seqlens.numel() > 2 else None
+    scratch = torch.empty(K.kpool_indexer_forward_host_scratch_size(
+        wl.T, wl.H, wl.D, wl.kpool, wl.index_topk, cu, fp8, chunk_rows), dtype=torch.uint8,
+        device="cuda")
+    out = K.kpool_indexer_forward_host(pin(inp.q), pin(inp.k), pin(inp.gate), pin(inp.ape),
+                                       pin(inp.w), wl.kpool, wl.index_topk, wl.tail, cu, fp8,
+                                       chunk_rows, scratch=scratch)
+    torch.cuda.synchronize()
+    assert K.kpool_read_status(scratch) == 0
+    return out
+
+
+@pytest.mark.parametrize("chunk_rows", [3000, 4093, 0])
+def test_single_sequence(K, chunk_rows):
+    wl = W.Workload("p1", T=20000, H=64, D=128, kpool=4, index_topk=512)
+    inp = W.make_inputs(wl, seed=31)
+    assert torch.equal(_host_tokens(K, inp, wl, False, chunk_rows), _device_tokens(K, inp, wl, False))
+
+
+def test_packed_documents_cut_by_chunks(K):
+    wl = W.Workload("p2", T=12000, H=32, D=64, kpool=4, index_topk=256, n_docs=7,
+                    doc_len_range=(100, 4000))
+    inp = W.make_inputs(wl, seed=32)
+    assert torch.equal(_host_tokens(K, inp, wl, False, 1000), _device_tokens(K, inp, wl, False))
+
+
+def test_fp8_mode(K):
+    wl = W.Workload("p3", T=9000, H=64, D=128, kpool=4, index_topk=1024, fp8=True)
+    inp = W.make_inputs(wl, seed=33)
+    assert torch.equal(_host_tokens(K, inp, wl, True, 2500), _device_tokens(K, inp, wl, True))
+
+
+def test_no_tail_and_kpool_two(K):
+    wl = W.Workload("p4", T=5000, H=16, D=128, kpool=2, index_topk=256, tail=False, n_docs=3,
+                    doc_len_range=(500, 3000))
+    inp = W.make_inputs(wl, seed=34)
+    assert torch.equal(_host_tokens(K, inp, wl, False, 777), _device_tokens(K, inp, wl, False))
+
+
+def test_no_complete_pool(K):
+    wl = W.Workload("p5", T=3, H=4, D=32, kpool=4, index_topk=32)
+    inp = W.make_inputs(wl, seed=35)
+    out = _host_tokens(K, inp, wl, False, 0)
+    assert torch.equal(out, _device_tokens(K, inp, wl, False))
+    assert out[2, :3].tolist() == [0, 1, 2] and bool((out[:, 3:] == -1).all())
