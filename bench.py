@@ -324,7 +324,7 @@ def main():
     ap.add_argument("--workload", default="long_128k", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--baseline-rows", type=int, default=1536)
+    ap.add_argument("--baseline-rows", type=int, default=3584)
     ap.add_argument("--ref-rows", type=int, default=48)
     ap.add_argument("--T", type=int, default=None,
                     help="same recipe at another token count (profiling runs)")
