@@ -8,21 +8,22 @@
 // "GLM-5.3-Flash F5: NoPE DSA + KPool indexer": relu homogeneity lets any
 // head_dim^-0.5 factor live in w; DeepSelect-style radix selection).
 //
-// Design (one persistent CTA per SM, 12 warps):
+// Design (one persistent CTA per SM, 20 warps):
 //   warp 0      TMA producer + tile scheduler (atomic counter over a
-//               longest-first query-tile table built by schedule_kernel)
+//               longest-first unit table built by schedule_kernel, or by
+//               split_schedule_kernel for calls with few query tiles)
 //   warp 1      tcgen05.mma issuer (one thread)
 //   warp 2      TMEM allocator
-//   warps 4-11  epilogue: tcgen05.ld of the accumulator, relu * w head
-//               reduction, threshold filter, ordered append into per-query
-//               candidate buffers in shared memory, radix-select compaction.
-// MMA tile: M = 128 pools (TMEM lanes, one epilogue thread per pool),
-// N = 256 (query, head) columns = 256 / H queries, K = D (bf16: 16 per
-// instruction, E4M3: 32).  q of the query tile stays resident in shared
-// memory; pooled-key tiles stream through a ring of `stages` buffers; two
-// 256-column TMEM accumulators let the epilogue of tile i overlap the MMAs of
-// tile i+1.  Candidates are kept in ascending pool order, so ties resolve to
-// the lower pool index by position and no final sort is needed.
+//   warps 4-19  epilogue: tcgen05.ld of the accumulator, relu * w head
+//               reduction, threshold filter, unordered appends into per-query
+//               candidate areas in shared memory, radix-select compaction,
+//               final selection ranked into ascending pool order.
+// MMA tile: M = 128 pools (TMEM lanes, one epilogue thread per pool and
+// 64-column slice), N = 256 (query, head) columns = 256 / H queries, K = D
+// (bf16: 16 per instruction, E4M3: 32).  q of the query tile stays resident in
+// shared memory; pooled-key tiles stream through a ring of `stages` buffers;
+// two 256-column TMEM accumulators let the epilogue of tile i overlap the MMAs
+// of tile i+1.  Ties resolve to the lower pool index inside the selection.
 #include <cuda.h>
 
 #include <algorithm>
@@ -111,7 +112,7 @@ Layout make_layout(int H, int D, int fp8)
     Layout L{};
     const int esize = fp8 ? 1 : 2;
     L.n_kchunks = (D * esize + 127) / 128;
-    L.stages = fp8 ? 4 : 3;
+    L.stages = fp8 ? 4 : 2;   // bf16: two stages leave room for ~1000 more candidates per query
     const int QT = qt_of(H);
     L.q_chunk = kBN * 128;
     L.pk_chunk = kBM * 128;
@@ -897,8 +898,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int Kp = p.Kp;
         const int slack = max(0, min(kSlack, C - kBM - Kp));
         // tiles between capacity checks; a query above `room` candidates at a
-        // check is compacted, so the next G tiles (<= 128 each) always fit
-        const int G = max(1, min(4, (C - Kp - slack) / kBM));
+        // check is compacted, so the next G tiles (<= 128 each) always fit.  G
+        // takes at most half of the space above the kept Kp + slack.
+        const int G = max(1, min(8, (C - Kp - slack) / (2 * kBM)));
         const int room = C - G * kBM;
         const unsigned lt = (1u << lane) - 1u;
         int acc = 0, tile_seq = 0;
