@@ -165,34 +165,44 @@ def test_fullsize_decode_128x32k(K, ora):
 def _split_vs_unsplit(K, ora, wl, n_check):
     """kpool_score_topk_at with a workspace that enables the split-pool
     schedule against the same call with the minimal workspace (one unit per
-    query tile): identical outputs, bit for bit; plus oracle rows."""
+    query tile): identical outputs, bit for bit; plus oracle rows (in FP8 mode
+    on the GPU's own E4M3 codes and scales)."""
     dev = torch.device("cuda")
     inp = W.make_inputs(wl)
     cu_k = inp.cu_seqlens.numpy()
     n_docs = len(cu_k) - 1
     cu_pools_h, P = K.kpool_num_pools(inp.cu_seqlens, wl.T, wl.kpool)
     d_ck, d_cp = inp.cu_seqlens.to(dev), cu_pools_h.to(dev)
-    pk = K.kpool_compress(inp.k.to(dev), inp.gate.to(dev), inp.ape.to(dev), wl.kpool, d_ck, d_cp,
-                          P)
     d_cq, d_qp = inp.cu_q.to(dev), inp.q_pos.to(dev)
     q, w = inp.q.to(dev), inp.w.to(dev)
+    qs = pks = None
+    if wl.fp8:
+        pk_bf, pk, pks = K.kpool_compress(inp.k.to(dev), inp.gate.to(dev), inp.ape.to(dev),
+                                          wl.kpool, d_ck, d_cp, P, fp8=True)
+        q, qs = K.kpool_quantize_fp8(q)
+    else:
+        pk = K.kpool_compress(inp.k.to(dev), inp.gate.to(dev), inp.ape.to(dev), wl.kpool, d_ck,
+                              d_cp, P)
     Tq, H = inp.Tq, wl.H
     ws_split = K.new_workspace(Tq, H, n_docs, dev, wl.kpool, wl.index_topk)
     ws_one = K.new_workspace(Tq, H, n_docs, dev)
     assert ws_split.numel() > ws_one.numel()
-    a = K.kpool_score_topk_at(q, w, pk, wl.kpool, wl.index_topk, d_cq, d_qp, d_cp,
-                              workspace=ws_split)
-    b = K.kpool_score_topk_at(q, w, pk, wl.kpool, wl.index_topk, d_cq, d_qp, d_cp,
-                              workspace=ws_one)
+    a = K.kpool_score_topk_at(q, w, pk, wl.kpool, wl.index_topk, d_cq, d_qp, d_cp, q_scale=qs,
+                              pk_scale=pks, workspace=ws_split)
+    b = K.kpool_score_topk_at(q, w, pk, wl.kpool, wl.index_topk, d_cq, d_qp, d_cp, q_scale=qs,
+                              pk_scale=pks, workspace=ws_one)
     torch.cuda.synchronize()
     assert K.kpool_read_status(ws_split) == 0 and K.kpool_read_status(ws_one) == 0
     assert torch.equal(a[0], b[0])
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
-    from kpool_checks import bf16_bits
-    pkb = bf16_bits(pk)
     cq, qp = inp.cu_q.numpy(), inp.q_pos.numpy()
     rows = np.unique(np.linspace(0, Tq - 1, n_check).astype(np.int64))
-    ops = ora.Operands(W.bits(inp.q), inp.w.numpy(), pkb)
+    if wl.fp8:
+        ops = ora.Operands(q.cpu().numpy(), inp.w.numpy(), pk.cpu().numpy(), qs.cpu().numpy(),
+                           pks.cpu().numpy())
+    else:
+        from kpool_checks import bf16_bits
+        ops = ora.Operands(W.bits(inp.q), inp.w.numpy(), bf16_bits(pk))
 
     class At:
         select_rows = staticmethod(lambda ops_, cu, kp, Kp, r: ora.select_rows_at(
@@ -230,3 +240,20 @@ def test_split_schedule_small_heads_and_large_budget(K, ora):
     wl = W.Workload("split_kp2", T=4 * 12000, H=64, D=128, kpool=2, index_topk=2048,
                     n_docs=4, equal_docs=True, queries="last", seed=24)
     _split_vs_unsplit(K, ora, wl, 4)
+
+
+def test_split_schedule_decode_fp8(K, ora):
+    """Lone-query tiles in FP8 mode: the per-pool E4M3 scale in the packed
+    accumulator loop."""
+    wl = W.Workload("split_decode_fp8", T=24 * 16384, H=64, D=128, kpool=4, index_topk=2048,
+                    n_docs=24, doc_len_range=(4096, 28672), queries="last", fp8=True, seed=25)
+    idx = _split_vs_unsplit(K, ora, wl, 8)
+    assert np.all(idx >= 0)
+
+
+def test_split_schedule_decode_h128(K, ora):
+    """H = 128: two pool tiles per accumulator, each query's heads in two
+    64-column halves."""
+    wl = W.Workload("split_decode_h128", T=16 * 12000, H=128, D=64, kpool=4, index_topk=1024,
+                    n_docs=16, doc_len_range=(3000, 20000), queries="last", seed=26)
+    _split_vs_unsplit(K, ora, wl, 8)
