@@ -325,6 +325,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--baseline-rows", type=int, default=3584)
+    ap.add_argument("--e2e-chunk-rows", type=int, default=0,
+                    help="query rows per chunk of the end-to-end pass (0 = the library's default)")
     ap.add_argument("--ref-rows", type=int, default=48)
     ap.add_argument("--T", type=int, default=None,
                     help="same recipe at another token count (profiling runs)")
@@ -459,11 +461,12 @@ def main():
         h2d += hcu.numel() * 4 if multi else 0
         d2h = htok.numel() * htok.element_size()
         scratch = torch.empty(K.kpool_indexer_forward_host_scratch_size(
-            T, H, D, kp, topk, hcu, wl.fp8), dtype=torch.uint8, device=dev)
+            T, H, D, kp, topk, hcu, wl.fp8, args.e2e_chunk_rows), dtype=torch.uint8, device=dev)
 
         def e2e_step():
             K.kpool_indexer_forward_host(hq, hk, hg, ha, hw, kp, topk, wl.tail, hcu, wl.fp8,
-                                         scratch=scratch, out=htok, device=dev)
+                                         args.e2e_chunk_rows, scratch=scratch, out=htok,
+                                         device=dev)
 
         for _ in range(2):
             e2e_step()
@@ -485,7 +488,8 @@ def main():
         e2e = {"value": whole_job_rate(T, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
                "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "api": "kpool_indexer_forward_host (C ABI, pinned host buffers, copies "
-                      "overlapped with the kernels in 16384-row chunks)"}
+                      "overlapped with the kernels in query chunks of up to %d rows)"
+                      % (args.e2e_chunk_rows or 16384)}
         del hq, hk, hg, ha, hw, htok, scratch
 
     # ---- roofline of the dominant kernel ---------------------------------

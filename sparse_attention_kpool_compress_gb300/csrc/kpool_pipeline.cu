@@ -7,6 +7,9 @@
 // processed in chunks on three streams: copy-in of chunk c+1, scoring and
 // expansion of chunk c, and copy-out of chunk c-1 run at the same time, with
 // two device buffers for the copied q/w rows and two for the token indices.
+// Chunks ramp up in size at the start and down at the end (chunk_bounds).  (A
+// second compute stream, letting consecutive chunks' scoring kernels overlap,
+// was measured slower on long sequences and is not used.)
 // A chunk is scored as positioned queries over the global pooled keys (each
 // document's rows of the chunk start at their own position), so every query
 // gets exactly the result of the unchunked pass: scores and selections are per
@@ -81,6 +84,26 @@ int pipe_streams(PipeStreams **out)
 }
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Chunk boundaries over [0, T): sizes ramp up R/8, R/4, R/2 at the start and
+// down R/2, R/4, R/8 at the end, R in between, so that the first copy-in and
+// the last copy-out (which nothing overlaps) are short.
+std::vector<int64_t> chunk_bounds(int64_t T, int64_t R)
+{
+    std::vector<int64_t> head, tail;
+    int64_t lo = 0, hi = T;
+    for (int64_t s = std::max<int64_t>(R / 8, 1); s < R && hi - lo >= 2 * s; s *= 2) {
+        head.push_back(s);
+        tail.push_back(s);
+        lo += s;
+        hi -= s;
+    }
+    std::vector<int64_t> b{0};
+    for (int64_t s : head) b.push_back(b.back() + s);
+    while (hi - b.back() > 0) b.push_back(std::min(hi, b.back() + R));
+    for (auto it = tail.rbegin(); it != tail.rend(); ++it) b.push_back(b.back() + *it);
+    return b;
+}
 
 // Scratch layout (byte offsets, each 256-aligned).  The first 256 bytes are a
 // header whose int 1 is the sticky status (read by kpool_read_status).
@@ -190,10 +213,11 @@ int run_pipeline(const PipelineArgs &a, cudaStream_t stream)
                                      at(L.pk), a.fp8 ? static_cast<uint8_t *>(at(L.pk8)) : nullptr,
                                      a.fp8 ? static_cast<float *>(at(L.pks)) : nullptr, s_cmp));
 
-    const int64_t n_chunks = (T + R - 1) / R;
+    const std::vector<int64_t> bounds = chunk_bounds(T, R);
+    const int64_t n_chunks = static_cast<int64_t>(bounds.size()) - 1;
     for (int64_t c = 0; c < n_chunks; ++c) {
         const int b = static_cast<int>(c & 1);
-        const int64_t r0 = c * R, r1 = std::min(T, r0 + R), rows = r1 - r0;
+        const int64_t r0 = bounds[c], r1 = bounds[c + 1], rows = r1 - r0;
         // copy-in of the chunk's q and w rows once buffer b is free again
         if (c >= 2) KPOOL_CUDA_CHECK(cudaStreamWaitEvent(s_in, ps->ev_cmp[b], 0));
         KPOOL_CUDA_CHECK(cudaMemcpyAsync(
