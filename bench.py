@@ -62,8 +62,16 @@ def load_peaks():
 
 
 def file_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Fingerprint of a C/CUDA source: sha256 (16 hex digits) of its code with
+    comments removed and whitespace collapsed, so that comment edits keep a
+    recorded profile valid while any code change invalidates it."""
+    import re
+    with open(path, encoding="utf-8") as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    src = " ".join(src.split())
+    return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
 def recorded_traffic(kernel, workload):

@@ -223,7 +223,8 @@ __device__ __forceinline__ int pool_tiles_of(const TileInfo &ti, int QT, int kp)
 __device__ __forceinline__ void group_bar(int g) { ptx::named_bar_sync(2 + g, kGroupThreads); }
 
 // Radix search (DeepSelect-style, 8-bit digits) for the k-th largest of
-// keyf(e) over the entries e < n with partf(e), by one group of 64 threads.
+// keyf(e) over the entries e < n with partf(e), by one selection group
+// (kGroupThreads threads).
 // Digits start at the highest bit where the smallest and largest
 // participating key differ, so the first histogram is spread.  Results:
 //   kth    the k-th largest key, or (edge) the lower edge of the digit bin
@@ -334,7 +335,7 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
 }
 
 // Keep the k best of cs/ci[0..n), n > k (score descending, equal scores by
-// lower pool index), in place, by one group of 64 epilogue threads.  In prune
+// lower pool index), in place, by one selection group.  In prune
 // mode (exact = false) it may keep up to k + slack entries: all those at or
 // above a digit-bin edge.  Returns the number kept and writes to *thr_out the
 // key a later candidate (higher pool index) must exceed to possibly enter.
