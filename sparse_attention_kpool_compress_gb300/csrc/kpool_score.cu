@@ -61,7 +61,7 @@ constexpr int kRegsOther = 32, kRegsEpi = 112;
 constexpr int kSplitMaxQT = 1024;                     // query tiles it schedules, at most
 constexpr int64_t kSplitEntries = int64_t(1) << 21;   // (index, score) entries of partial lists
 constexpr int kSplitMaxSplits = 16;                   // units per query tile, at most
-constexpr int kSplitMinTiles = 4;                     // pool tiles per unit, at least
+constexpr int kSplitMinTiles = 32;                    // pool tiles per unit, at least
 
 // Optional phase timers (build with -DKPOOL_PHASE_TIMERS): per-role cycle
 // counts of waits and work, summed over all CTAs into g_phase_timers and read

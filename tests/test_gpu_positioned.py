@@ -162,7 +162,7 @@ def test_fullsize_decode_128x32k(K, ora):
     assert inp.Tq == 128 and np.all(idx >= 0)
 
 
-def _split_vs_unsplit(K, ora, wl, n_check):
+def _split_vs_unsplit(K, ora, wl, n_check, expect_split=True):
     """kpool_score_topk_at with a workspace that enables the split-pool
     schedule against the same call with the minimal workspace (one unit per
     query tile): identical outputs, bit for bit; plus oracle rows (in FP8 mode
@@ -193,6 +193,12 @@ def _split_vs_unsplit(K, ora, wl, n_check):
                               pk_scale=pks, workspace=ws_one)
     torch.cuda.synchronize()
     assert K.kpool_read_status(ws_split) == 0 and K.kpool_read_status(ws_one) == 0
+    # the workspace header's third word is the number of scheduled units: more
+    # units than query tiles means some tile's pools were split
+    qt = 256 // H
+    tiles = int(sum((int(n) + qt - 1) // qt for n in np.diff(inp.cu_q.numpy())))
+    units = int(ws_split[:12].view(torch.int32)[2])
+    assert (units > tiles) == expect_split, (units, tiles)
     assert torch.equal(a[0], b[0])
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
     cq, qp = inp.cu_q.numpy(), inp.q_pos.numpy()
@@ -232,14 +238,19 @@ def test_split_schedule_chunks_share_units(K, ora):
 
 
 def test_split_schedule_small_heads_and_large_budget(K, ora):
-    """H = 16 (16 queries per tile) with Kp = 256, and kpool = 2 with Kp = 1024
-    (too large to merge in place: the call runs unsplit)."""
-    wl = W.Workload("split_h16", T=8 * 6000, H=16, D=64, kpool=4, index_topk=1024,
+    """H = 16 (16 queries per tile) with Kp = 256; kpool = 2 with Kp = 1024 (split,
+    larger partial lists); kpool = 1 with Kp = 1536, more than half a query's
+    candidate capacity, so the lists cannot be merged in place and the call runs
+    unsplit."""
+    wl = W.Workload("split_h16", T=8 * 24000, H=16, D=64, kpool=4, index_topk=1024,
                     n_docs=8, equal_docs=True, queries="chunk:21", seed=23)
     _split_vs_unsplit(K, ora, wl, 16)
     wl = W.Workload("split_kp2", T=4 * 12000, H=64, D=128, kpool=2, index_topk=2048,
                     n_docs=4, equal_docs=True, queries="last", seed=24)
     _split_vs_unsplit(K, ora, wl, 4)
+    wl = W.Workload("split_kp1", T=4 * 12000, H=64, D=128, kpool=1, index_topk=1536,
+                    n_docs=4, equal_docs=True, queries="last", seed=27)
+    _split_vs_unsplit(K, ora, wl, 4, expect_split=False)
 
 
 def test_split_schedule_decode_fp8(K, ora):
