@@ -107,12 +107,13 @@ struct Layout {
 
 __host__ __device__ inline int qt_of(int H) { return kBN / H; }
 
-Layout make_layout(int H, int D, int fp8)
+Layout make_layout(int H, int D, int fp8, int stages = 0)
 {
     Layout L{};
     const int esize = fp8 ? 1 : 2;
     L.n_kchunks = (D * esize + 127) / 128;
     L.stages = fp8 ? 4 : 2;   // bf16: two stages leave room for ~1000 more candidates per query
+    if (stages > 0) L.stages = stages;
     const int QT = qt_of(H);
     L.q_chunk = kBN * 128;
     L.pk_chunk = kBM * 128;
@@ -1611,7 +1612,14 @@ int run_score(const ScoreArgs &a, cudaStream_t s)
         KPOOL_CUDA_CHECK(cudaGetLastError());
         return KPOOL_OK;
     }
-    const Layout L = make_layout(a.H, a.D, a.fp8);
+    // few query tiles (decode, short chunks) with room in the workspace: split
+    // their pool lists over the CTAs (C >= 2 Kp lets a merge append a whole
+    // partial list after at most one compaction).  That instantiation streams
+    // pooled keys through one more stage: its units are memory-bound.
+    const SplitLayout SL = split_layout(a.T, a.H, a.n_docs, a.Kp);
+    const Layout Lf = make_layout(a.H, a.D, a.fp8, a.fp8 ? 4 : 3);
+    const bool split = a.mode == 0 && SL.ok && a.ws_bytes >= SL.bytes && Lf.C >= 2 * a.Kp;
+    const Layout L = split ? Lf : make_layout(a.H, a.D, a.fp8);
     CUtensorMap mq, mpk;
     int rc = encode_2d(&mq, a.q, a.fp8, static_cast<uint64_t>(a.D),
                        static_cast<uint64_t>(a.T) * a.H, kBN);
@@ -1643,11 +1651,6 @@ int run_score(const ScoreArgs &a, cudaStream_t s)
     prm.idesc = ptx::make_idesc(a.fp8 ? 0u : 1u, kBM, kBN);
     prm.L = L;
 
-    // few query tiles (decode, short chunks) with room in the workspace: split
-    // their pool lists over the CTAs; C >= 2 Kp lets a merge append a whole
-    // partial list after at most one compaction
-    const SplitLayout SL = split_layout(a.T, a.H, a.n_docs, a.Kp);
-    const bool split = a.mode == 0 && SL.ok && a.ws_bytes >= SL.bytes && L.C >= 2 * a.Kp;
     int grid;
     if (split) {
         prm.units = a.ws + SL.units_off;

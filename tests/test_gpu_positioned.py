@@ -238,17 +238,17 @@ def test_split_schedule_chunks_share_units(K, ora):
 
 
 def test_split_schedule_small_heads_and_large_budget(K, ora):
-    """H = 16 (16 queries per tile) with Kp = 256; kpool = 2 with Kp = 1024 (split,
-    larger partial lists); kpool = 1 with Kp = 1536, more than half a query's
-    candidate capacity, so the lists cannot be merged in place and the call runs
-    unsplit."""
+    """H = 16 (16 queries per tile) with Kp = 256; kpool = 2 with Kp = 768 (split,
+    larger partial lists); kpool = 2 with Kp = 1024, more than half a query's
+    candidate capacity in the split layout, so the lists cannot be merged in
+    place and the call runs unsplit."""
     wl = W.Workload("split_h16", T=8 * 24000, H=16, D=64, kpool=4, index_topk=1024,
                     n_docs=8, equal_docs=True, queries="chunk:21", seed=23)
     _split_vs_unsplit(K, ora, wl, 16)
-    wl = W.Workload("split_kp2", T=4 * 12000, H=64, D=128, kpool=2, index_topk=2048,
+    wl = W.Workload("split_kp2", T=4 * 12000, H=64, D=128, kpool=2, index_topk=1536,
                     n_docs=4, equal_docs=True, queries="last", seed=24)
     _split_vs_unsplit(K, ora, wl, 4)
-    wl = W.Workload("split_kp1", T=4 * 12000, H=64, D=128, kpool=1, index_topk=1536,
+    wl = W.Workload("split_kp2_big", T=4 * 12000, H=64, D=128, kpool=2, index_topk=2048,
                     n_docs=4, equal_docs=True, queries="last", seed=27)
     _split_vs_unsplit(K, ora, wl, 4, expect_split=False)
 
