@@ -367,3 +367,26 @@ def test_status_clean_and_bad_seqlens(K):
     cp = torch.tensor([0, 50, 25], dtype=torch.int32, device="cuda")
     K.kpool_score_topk(q, w, pk, 4, 32, cu, cp, workspace=ws)
     assert K.kpool_read_status(ws) & K.STATUS_BAD_SEQLENS
+
+
+def test_fp8_chain_hand_worked_onehot_gpu(K):
+    """kpool_quantize_fp8 on the one-hot rows of tests/golden/fp8_onehot_worked.txt:
+    the hand-worked codes and scales, including an exact E4M3 tie; and the same
+    rows as pooled keys (a pool of identical keys compresses to that key)."""
+    from test_oracle_pins import _fp8_onehot_cases, _fp8_onehot_expected
+    cases = _fp8_onehot_cases()
+    x = torch.zeros(len(cases), 128, dtype=torch.float32)
+    for r, (v, j, _, _, _) in enumerate(cases):
+        x[r, j] = v
+    xb = x.to(torch.bfloat16)
+    codes, scales = K.kpool_quantize_fp8(dev(xb))
+    # pooled keys: kpool = 2, both slots of pool r hold row r
+    k = xb.repeat_interleave(2, dim=0)
+    _, pk8, pks = K.kpool_compress(dev(k), dev(torch.zeros_like(k)), dev(torch.zeros(2, 128)), 2,
+                                   fp8=True)
+    torch.cuda.synchronize()
+    for got_c, got_s in ((codes.cpu().numpy(), scales.cpu().numpy()),
+                         (pk8.cpu().numpy(), pks.cpu().numpy())):
+        for r, (v, j, e, cpos, cneg) in enumerate(cases):
+            assert got_s[r] == 2.0 ** e, (v, j, got_s[r])
+            assert np.array_equal(got_c[r], _fp8_onehot_expected(v, j, cpos, cneg)), (v, j)

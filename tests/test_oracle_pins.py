@@ -572,3 +572,33 @@ def test_decode_queries_see_their_document_prefix(ora):
     far = ora.select_rows_at(ops_d, cq, qpos + 1000, cu, wl.kpool, 1000, np.arange(3))
     cp = ora.cu_pools(cu, wl.kpool)
     assert list(far["n_sel"]) == list(np.diff(cp))
+
+
+def _fp8_onehot_cases():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "fp8_onehot_worked.txt")
+    cases = []
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        v, j, e, cpos, cneg = line.split()
+        cases.append((float(v), int(j), int(e), int(cpos, 16), int(cneg, 16)))
+    return cases
+
+
+def _fp8_onehot_expected(v, j, cpos, cneg):
+    signs = np.array([(-1) ** bin(i & j).count("1") for i in range(128)]) * np.sign(v)
+    return np.where(signs > 0, cpos, cneg).astype(np.uint8)
+
+
+def test_fp8_chain_hand_worked_onehot(ora):
+    """One-hot rows through the FP8 input path: codes and scales worked out by
+    hand (tests/golden/fp8_onehot_worked.txt), including an exact E4M3 tie."""
+    cases = _fp8_onehot_cases()
+    x = torch.zeros(len(cases), 128, dtype=torch.float32)
+    for r, (v, j, _, _, _) in enumerate(cases):
+        x[r, j] = v
+    codes, scales = ora.fp8_rows(W.bits(x.to(torch.bfloat16)))
+    for r, (v, j, e, cpos, cneg) in enumerate(cases):
+        assert scales[r] == 2.0 ** e, (v, j, scales[r])
+        assert np.array_equal(codes[r], _fp8_onehot_expected(v, j, cpos, cneg)), (v, j)
