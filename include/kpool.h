@@ -15,8 +15,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every pointer argument is a DEVICE pointer owned by the caller unless
- *    its name ends in _host.  The library never allocates device memory and
- *    never frees what it is given.
+ *    its name, or the function's, ends in _host (kpool_indexer_forward_host
+ *    takes host buffers and a device scratch).  The library never allocates
+ *    device memory and never frees what it is given; the host-buffer pass
+ *    creates its streams and events once per host thread and device.
  *  - Each call enqueues its kernels on `stream` (NULL = legacy default
  *    stream) and returns without synchronising.  Results are valid once the
  *    stream has reached that point.
@@ -145,7 +147,8 @@ KPOOL_API size_t kpool_score_topk_workspace_size(int64_t T, int H, int n_docs);
  * lets kpool_score_topk / kpool_score_topk_at split long pool lists over
  * several CTAs when a call has few query tiles (decode batches, short
  * chunks: at most 1024 tiles of 256 / H rows).  Each query tile's pools are
- * then scored in units on different SMs; every unit keeps its own best Kp
+ * then scored in units (of at least 32 pool tiles) on different SMs, provided
+ * 2 * Kp fits the per-query candidate capacity; every unit keeps its own best Kp
  * (the same scores, the same order: score descending, ties to the lower
  * pool index) and the last unit to finish merges them, so the outputs are
  * identical to the unsplit schedule's.  Equal to
@@ -296,9 +299,10 @@ KPOOL_API int kpool_expand_indices(const int32_t *pool_idx, const int32_t *cu_se
  * HOST token indices (Megatron-LM PR section 3: compression, pool top-k,
  * expansion with the causal tail, packed THD; the FP8 input path), with the
  * host<->device copies overlapped with the kernels.  Keys are copied and
- * compressed first; the query rows then go in chunks of chunk_rows (0 =
- * 16384) over three internal streams: the copy-in of chunk c+1, the scoring
- * and expansion of chunk c and the copy-out of chunk c-1 run concurrently.
+ * compressed first; the query rows then go in chunks of up to chunk_rows
+ * (0 = 16384; the first and last chunks ramp from chunk_rows / 8) over three
+ * internal streams: the copy-in of chunk c+1, the scoring and expansion of
+ * chunk c and the copy-out of chunk c-1 run concurrently.
  * Each chunk is scored as positioned queries over the global pooled keys, so
  * tok_idx_out equals what kpool_compress -> [kpool_quantize_fp8] ->
  * kpool_score_topk -> kpool_expand_indices give on the same inputs.
