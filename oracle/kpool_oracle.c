@@ -25,7 +25,7 @@
  *         commit notes: relu homogeneity (head_dim^-0.5 movable into w);
  *         causal [start, end) pool ranges.
  *
- * Readings of points the pages leave open (each is listed in the design doc):
+ * Readings of points the pages leave open:
  *   - A pool is a candidate for query t iff its last token is <= t
  *     (complete causal pools); the tail is t's own pool only when that pool
  *     is incomplete at t, i.e. (tau+1) mod kp != 0.
