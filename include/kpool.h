@@ -205,7 +205,11 @@ KPOOL_API int kpool_score_topk(const void *q, const float *q_scale, const float 
  * pk[cu_pools[d] .. cu_pools[d+1]) (from kpool_compress on the keys).  A query
  * at position tau scores the complete pools j < floor((tau+1)/kpool), clamped
  * to the document's pools.  With q_start_pos = 0 and the keys' cu_seqlens as
- * cu_seqlens_q this is kpool_score_topk.  All three index arrays are device
+ * cu_seqlens_q this is kpool_score_topk.  The caller keeps every position
+ * inside its document (q_start_pos[d] + rows_d <= the document's key count);
+ * the device does not check it (pools clamp to the document's, but the tail
+ * tokens kpool_expand_indices_at writes for a position past the keys would
+ * point past them).  All three index arrays are device
  * int32 and required; Tq = cu_seqlens_q[n_docs]; the workspace is sized by
  * kpool_score_topk_workspace_size(Tq, H, n_docs), or by
  * kpool_score_topk_workspace_size_split(Tq, H, n_docs, kpool, index_topk)

@@ -350,7 +350,9 @@ def kpool_indexer_forward_host(q, k, gate, ape, w, kpool: int, index_topk: int,
     """The whole pass from host (CPU, ideally pinned) tensors to host token
     indices int32 [T, Kp*kpool + kpool - 1], copies overlapped with the
     kernels.  Enqueued on the current CUDA stream of `device`; synchronize it
-    before reading the result."""
+    before reading the result.  Without `scratch`, a device scratch of
+    kpool_indexer_forward_host_scratch_size bytes (about 0.9 GB at T=131072)
+    is allocated for the call: pass one to reuse it across calls."""
     for t_, n_, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16),
                        (gate, "gate", torch.bfloat16), (ape, "ape", torch.float32),
                        (w, "w", torch.float32)):
