@@ -81,3 +81,20 @@ def test_no_complete_pool(K):
     out = _host_tokens(K, inp, wl, False, 0)
     assert torch.equal(out, _device_tokens(K, inp, wl, False))
     assert out[2, :3].tolist() == [0, 1, 2] and bool((out[:, 3:] == -1).all())
+
+
+def test_packed_documents_fp8(K):
+    """Packed documents and FP8 mode together: the per-chunk q quantisation and
+    the per-document pooled-key scales across chunk boundaries."""
+    wl = W.Workload("p6", T=10000, H=64, D=128, kpool=4, index_topk=512, n_docs=5,
+                    doc_len_range=(500, 4000), fp8=True)
+    inp = W.make_inputs(wl, seed=36)
+    assert torch.equal(_host_tokens(K, inp, wl, True, 1500), _device_tokens(K, inp, wl, True))
+
+
+def test_two_queries_per_warp_packed(K):
+    """H = 32 (two queries per epilogue warp), packed documents, chunks of 999."""
+    wl = W.Workload("p7", T=9000, H=32, D=128, kpool=4, index_topk=1024, n_docs=4,
+                    doc_len_range=(800, 4000))
+    inp = W.make_inputs(wl, seed=37)
+    assert torch.equal(_host_tokens(K, inp, wl, False, 999), _device_tokens(K, inp, wl, False))
