@@ -60,3 +60,36 @@ def test_chunk_compress_plan():
     inp = W.make_inputs(W.Workload("d", T=64, H=2, D=32, kpool=4, index_topk=8, n_docs=2,
                                    equal_docs=True, queries="last"))
     assert bench.chunk_compress_plan(inp) is None
+
+
+def test_source_fingerprint_ignores_comments(tmp_path):
+    import bench
+    a = tmp_path / "a.cu"
+    b = tmp_path / "b.cu"
+    c = tmp_path / "c.cu"
+    a.write_text("int f(int x) {\n  return x + 1;  // one\n}\n")
+    b.write_text("/* header */\nint f(int x)\n{\n    return x + 1;\n}\n")
+    c.write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.file_hash(str(a)) == bench.file_hash(str(b))
+    assert bench.file_hash(str(a)) != bench.file_hash(str(c))
+
+
+def test_reference_arm_positioned_workload(capsys, monkeypatch):
+    """The oracle arm on a tiny decode-style workload: one JSON line with the
+    reference fields (the oracle times selection and expansion of the rows)."""
+    import json
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+
+    class A:
+        steps = 1
+        warmup = 3
+        ref_rows = 8
+    wl = W.Workload("tiny_decode", T=600, H=4, D=32, kpool=4, index_topk=32, n_docs=3,
+                    doc_len_range=(100, 300), queries="last")
+    assert bench.run_reference(A(), wl) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert "pooled-key cache" in line["cpu_baseline"]["sample"]
