@@ -390,3 +390,19 @@ def test_fp8_chain_hand_worked_onehot_gpu(K):
         for r, (v, j, e, cpos, cneg) in enumerate(cases):
             assert got_s[r] == 2.0 ** e, (v, j, got_s[r])
             assert np.array_equal(got_c[r], _fp8_onehot_expected(v, j, cpos, cneg)), (v, j)
+
+
+def test_score_and_selection_hand_worked_gpu(K):
+    """tests/golden/score_select_worked.txt padded to H = 4 (w = 0 on the extra
+    heads) and D = 32 (zeros): the hand-worked scores, selections and the tie to
+    the lower pool index, exactly; kpool = 1 so pk = k and tokens = pools."""
+    from test_oracle_pins import score_select_worked
+    q, k, w, want_idx, want_sc = score_select_worked(pad_heads=4, pad_dims=32)
+    pk = K.kpool_compress(dev(k), dev(torch.zeros_like(k)), dev(torch.zeros(1, 32)), 1)
+    idx, sc = K.kpool_score_topk(dev(q), dev(w), pk, 1, 2)
+    tok = K.kpool_expand_indices(idx, 1, 2, True)
+    torch.cuda.synchronize()
+    assert torch.equal(pk.cpu(), k)
+    assert np.array_equal(idx.cpu().numpy(), want_idx)
+    assert np.array_equal(sc.cpu().numpy().astype(np.float64), want_sc)
+    assert np.array_equal(tok.cpu().numpy(), want_idx)

@@ -602,3 +602,35 @@ def test_fp8_chain_hand_worked_onehot(ora):
     for r, (v, j, e, cpos, cneg) in enumerate(cases):
         assert scales[r] == 2.0 ** e, (v, j, scales[r])
         assert np.array_equal(codes[r], _fp8_onehot_expected(v, j, cpos, cneg)), (v, j)
+
+
+def score_select_worked(pad_heads=2, pad_dims=2):
+    """The hand-worked fixture tests/golden/score_select_worked.txt as bf16
+    inputs, optionally zero-padded to more heads (w = 0) and dimensions."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "score_select_worked.txt")
+    lines = [ln for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    kv = [float(x) for x in lines[0].split(":")[1].split()]
+    k = torch.zeros(5, pad_dims)
+    k[:, :2] = torch.tensor(kv).view(5, 2)
+    q = torch.zeros(5, pad_heads, pad_dims)
+    q[:, 0, 0] = 1.0
+    q[:, 1, 1] = 2.0
+    w = torch.zeros(5, pad_heads)
+    w[:, 0] = 1.0
+    w[:, 1] = -0.5
+    want_idx, want_sc = [], []
+    for ln in lines[1:]:
+        idx, sc = ln.split(":")[1].split("|")
+        want_idx.append([int(x) for x in idx.split()])
+        want_sc.append([float(x) for x in sc.split()])
+    return (q.to(torch.bfloat16), k.to(torch.bfloat16), w, np.array(want_idx, np.int32),
+            np.array(want_sc, np.float64))
+
+
+def test_score_and_selection_hand_worked(ora):
+    q, k, w, want_idx, want_sc = score_select_worked()
+    ops = ora.Operands(W.bits(q), w.numpy(), W.bits(k))
+    o = ora.select_rows(ops, None, 1, 2, np.arange(5))
+    assert np.array_equal(o["sel"], want_idx)
+    got = np.where(want_idx >= 0, o["sel_score"], -np.inf)
+    assert np.array_equal(got, want_sc)
