@@ -406,3 +406,21 @@ def test_score_and_selection_hand_worked_gpu(K):
     assert np.array_equal(idx.cpu().numpy(), want_idx)
     assert np.array_equal(sc.cpu().numpy().astype(np.float64), want_sc)
     assert np.array_equal(tok.cpu().numpy(), want_idx)
+
+
+@pytest.mark.parametrize("kp", [2, 3, 4])
+@pytest.mark.parametrize("D", [32, 128])
+def test_compress_hand_worked_moderate_logits_gpu(K, kp, D):
+    """kpool_compress on the hand-worked pools of tests/golden/compress_worked.txt
+    (softmax weights 1/4, 3/4, 1/8, 0.1 .. 0.4 at moderate logits): the pooled
+    keys equal the hand-derived BF16 values exactly, on the plain and on the
+    FP8-output path (whose BF16 pooled key is the same)."""
+    from test_oracle_pins import compress_worked_inputs
+    kb, gb, ape, want = compress_worked_inputs(kp, D)
+    pk = K.kpool_compress(dev(kb), dev(gb), dev(torch.from_numpy(ape)), kp)
+    torch.cuda.synchronize()
+    assert np.array_equal(pk.float().cpu().numpy()[0].astype(np.float64), want)
+    if D == 128:
+        pk2, _, _ = K.kpool_compress(dev(kb), dev(gb), dev(torch.from_numpy(ape)), kp, fp8=True)
+        torch.cuda.synchronize()
+        assert torch.equal(pk2.cpu(), pk.cpu())

@@ -634,3 +634,52 @@ def test_score_and_selection_hand_worked(ora):
     assert np.array_equal(o["sel"], want_idx)
     got = np.where(want_idx >= 0, o["sel_score"], -np.inf)
     assert np.array_equal(got, want_sc)
+
+
+def compress_worked_cases():
+    """tests/golden/compress_worked.txt: one hand-worked pool per line (kpool,
+    gate and keys per slot, ape = float32(ln m + c) per slot, the pooled key)."""
+    cases = []
+    for line in open(os.path.join(GOLDEN, "compress_worked.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        f = [x.split() for x in line.split("|")]
+        kp = int(f[0][0])
+        gate, m, c, keys = ([float(v) for v in f[i]] for i in range(1, 5))
+        assert len(gate) == len(m) == len(c) == len(keys) == kp
+        cases.append((kp, gate, m, c, keys, float(f[5][0])))
+    return cases
+
+
+def compress_worked_inputs(kp, D=32):
+    """The fixture's cases of one kpool laid out as one pool of D dimensions,
+    case i in dimension i, zeros elsewhere (whose pooled key is 0).  Returns
+    bf16 k and gate [kp, D] (torch), ape [kp, D] float32 and the expected
+    pooled keys [D] (float64)."""
+    cases = [cs for cs in compress_worked_cases() if cs[0] == kp]
+    assert 0 < len(cases) <= D
+    k = torch.zeros(kp, D)
+    gate = torch.zeros(kp, D)
+    ape = np.zeros((kp, D), np.float32)
+    want = np.zeros(D)
+    for d, (_, g, m, c, keys, pk) in enumerate(cases):
+        for s in range(kp):
+            k[s, d] = keys[s]
+            gate[s, d] = g[s]
+            ape[s, d] = np.float32(math.log(m[s]) + c[s])
+        want[d] = pk
+    kb, gb = k.to(torch.bfloat16), gate.to(torch.bfloat16)
+    assert torch.equal(kb.float(), k) and torch.equal(gb.float(), gate)   # BF16-exact inputs
+    return kb, gb, ape, want
+
+
+@pytest.mark.parametrize("kp", [2, 3, 4])
+def test_compress_hand_worked_moderate_logits(ora, kp):
+    """Hand-worked pooled keys at moderate logits (tests/golden/compress_worked.txt):
+    softmax weights that are small rationals (1/4, 3/4, 1/8, 0.1 .. 0.4), so a
+    softmax at another temperature, of the negated logits, over reversed slots,
+    or without the gate or the ape term gives another pooled key."""
+    kb, gb, ape, want = compress_worked_inputs(kp)
+    pk = ora.compress(W.bits(kb), W.bits(gb), ape, None, kp)
+    assert pk.shape == (1, 32)
+    assert np.array_equal(bf16_val(pk[0]), want), (bf16_val(pk[0]), want)
