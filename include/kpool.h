@@ -259,8 +259,13 @@ KPOOL_API int kpool_expand_indices_at(const int32_t *pool_idx, const int32_t *cu
  *     everything it reads from it before use, but calls that overlap on the
  *     GPU (different streams, or host threads) race on it and must be
  *     serialised by the caller.
- *   - The status word it writes is not exposed; validate cu_seqlens on the
- *     host (kpool_num_pools) when its values are untrusted.
+ *   - Its status word (malformed cu_seqlens, an expired pipeline wait) is
+ *     read with kpool_score_topk_noalloc_status.
+ *   - It always runs the unsplit schedule (one unit per query tile): the
+ *     fixed array has no room for the split-pool tables, so decode-sized
+ *     calls (few query tiles over long documents) run on fewer SMs and more
+ *     slowly than kpool_score_topk given a split-sized workspace.  Results
+ *     are the same.
  */
 KPOOL_API int kpool_score_topk_noalloc(const void *q, const float *q_scale, const float *w,
                                        const void *pk, const float *pk_scale,
@@ -268,6 +273,18 @@ KPOOL_API int kpool_score_topk_noalloc(const void *q, const float *q_scale, cons
                                        int n_docs, int64_t T, int64_t P_total, int H, int D,
                                        int kpool, int index_topk, int fp8, int32_t *pool_idx_out,
                                        float *pool_score_out, kpool_stream_t stream);
+
+/*
+ * kpool_score_topk_noalloc_status -- the status word (KPOOL_STATUS_* bits, 0 =
+ * clean) that the last kpool_score_topk_noalloc on the current device left in
+ * the library's fixed scratch: KPOOL_STATUS_BAD_SEQLENS when the device
+ * cu_seqlens were malformed (nothing was written to the outputs),
+ * KPOOL_STATUS_TIMEOUT when a pipeline wait gave up (outputs invalid).
+ * Synchronises the whole device, like kpool_read_status.  Allocates nothing.
+ * (The pages have no counterpart: it belongs to the allocation-free entry
+ * point.)
+ */
+KPOOL_API int kpool_score_topk_noalloc_status(int *status_out);
 
 /*
  * kpool_score_dense -- test/debug entry: the same scoring as
@@ -344,6 +361,20 @@ KPOOL_API int kpool_indexer_forward_host(const void *q, const void *k, const voi
  * Synchronises the whole device.
  */
 KPOOL_API int kpool_read_status(const void *workspace, int *status_out);
+
+/*
+ * kpool_debug_set_wait_limit_ns -- test entry: the time limit of each wait
+ * inside the scoring kernel (kpool_score_topk, _at, _noalloc, _dense and the
+ * host-buffer pass) for launches made after this call, process-wide; ns = 0
+ * restores the default of 2 s.  Returns the previous limit.  A wait that
+ * runs out sets KPOOL_STATUS_TIMEOUT in the call's status word and raises an
+ * abort flag in its CTA: the CTA's roles stop waiting, let their in-flight
+ * copies and MMAs land (bounded by 2 s whatever this limit), free their
+ * tensor memory and exit, and the outputs of that call are invalid.  Meant
+ * for tests of that path; production code leaves the default.  (The pages
+ * have no counterpart.)
+ */
+KPOOL_API uint64_t kpool_debug_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -55,6 +55,8 @@ _SIGS = {
                                  _P, _P, _P, _SZ, _P]),
     "kpool_expand_indices_at": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _P, _P]),
     "kpool_read_status": (_I, [_P, _P]),
+    "kpool_score_topk_noalloc_status": (_I, [_P]),
+    "kpool_debug_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "kpool_indexer_forward_host_scratch_size": (_SZ, [_P, _I, _L, _I, _I, _I, _I, _I, _L]),
     "kpool_indexer_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _I, _I, _I,
                                         _L, _P, _P, _SZ, _P]),
@@ -381,6 +383,20 @@ def kpool_read_status(workspace) -> int:
     v = ctypes.c_int(0)
     _check(_lib.kpool_read_status(_ptr(workspace), ctypes.byref(v)), "kpool_read_status")
     return int(v.value)
+
+
+def kpool_score_topk_noalloc_status() -> int:
+    """Status word of the last kpool_score_topk_noalloc on the current device."""
+    v = ctypes.c_int(0)
+    _check(_lib.kpool_score_topk_noalloc_status(ctypes.byref(v)),
+           "kpool_score_topk_noalloc_status")
+    return int(v.value)
+
+
+def kpool_debug_set_wait_limit_ns(ns: int) -> int:
+    """Test entry: limit of each scoring-kernel wait (0 = the 2 s default);
+    returns the previous limit."""
+    return int(_lib.kpool_debug_set_wait_limit_ns(int(ns)))
 
 
 def kpool_indexer_forward(q, k, gate, ape, w, kpool: int, index_topk: int,

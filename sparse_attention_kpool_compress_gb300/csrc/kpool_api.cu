@@ -160,6 +160,7 @@ int kpool_cu_pools(const int32_t *cu_seqlens, int n_docs, int kpool, int32_t *cu
                    kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_cu_pools");
     if (kpool < 1 || kpool > 64) return fail(KPOOL_ERR_UNSUPPORTED, "kpool must be in [1, 64]");
     if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1");
     if (!cu_seqlens || !cu_pools_out) return fail(KPOOL_ERR_INVALID_ARG, "NULL pointer");
@@ -174,6 +175,7 @@ int kpool_compress(const void *k, const void *gate, const float *ape,
                    uint8_t *pk_fp8_out, float *pk_scale_out, kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_compress");
     int rc = check_common(T, kpool);
     if (rc) return rc;
     if (D != 32 && D != 64 && D != 128)
@@ -201,6 +203,7 @@ int kpool_quantize_fp8(const void *x, int64_t rows, int D, uint8_t *x_fp8_out, f
                        kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_quantize_fp8");
     if (D != 128) return fail(KPOOL_ERR_UNSUPPORTED, "FP8 rows need D = 128 (got %d)", D);
     if (rows < 0) return fail(KPOOL_ERR_INVALID_ARG, "rows < 0");
     if (rows > 0 && (!x || !x_fp8_out || !scale_out))
@@ -233,6 +236,7 @@ int kpool_score_topk(const void *q, const float *q_scale, const float *w, const 
                      void *workspace, size_t workspace_bytes, kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_score_topk");
     int rc = check_score_args(q, q_scale, w, pk, pk_scale, cu_seqlens, cu_pools, n_docs, T,
                               P_total, H, D, kpool, fp8, workspace, workspace_bytes);
     if (rc) return rc;
@@ -266,6 +270,7 @@ int kpool_score_topk_noalloc(const void *q, const float *q_scale, const float *w
                              int32_t *pool_idx_out, float *pool_score_out, kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_score_topk_noalloc");
     int rc = check_common(T, kpool);
     if (rc) return rc;
     if ((rc = check_h(H))) return rc;
@@ -300,6 +305,7 @@ int kpool_score_topk_at(const void *q, const float *q_scale, const float *w, con
                         size_t workspace_bytes, kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_score_topk_at");
     if (!cu_seqlens_q || !q_start_pos || !cu_pools)
         return fail(KPOOL_ERR_INVALID_ARG, "cu_seqlens_q, q_start_pos and cu_pools are required");
     if (!aligned(q_start_pos, 4)) return fail(KPOOL_ERR_INVALID_ARG, "q_start_pos misaligned");
@@ -338,6 +344,7 @@ int kpool_expand_indices_at(const int32_t *pool_idx, const int32_t *cu_seqlens_q
                             kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_expand_indices_at");
     int rc = check_common(Tq, kpool);
     if (rc) return rc;
     if (!cu_seqlens_q || !q_start_pos || !cu_seqlens_k || !cu_pools)
@@ -367,6 +374,7 @@ int kpool_score_dense(const void *q, const float *q_scale, const float *w, const
                       kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_score_dense");
     int rc = check_score_args(q, q_scale, w, pk, pk_scale, cu_seqlens, cu_pools, n_docs, T,
                               P_total, H, D, kpool, fp8, workspace, workspace_bytes);
     if (rc) return rc;
@@ -390,6 +398,7 @@ int kpool_expand_indices(const int32_t *pool_idx, const int32_t *cu_seqlens,
                          kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_expand_indices");
     int rc = check_common(T, kpool);
     if (rc) return rc;
     if (index_topk < 1 || index_topk % kpool != 0)
@@ -476,6 +485,7 @@ int kpool_indexer_forward_host(const void *q, const void *k, const void *gate, c
                                kpool_stream_t stream)
 {
     clear_error();
+    KPOOL_NVTX_RANGE("kpool_indexer_forward_host");
     int rc = check_forward_shapes(T, H, D, kpool, index_topk, fp8);
     if (rc) return rc;
     if (chunk_rows < 0) return fail(KPOOL_ERR_INVALID_ARG, "chunk_rows < 0");
@@ -522,5 +532,19 @@ int kpool_read_status(const void *workspace, int *status_out)
     *status_out = v;
     return KPOOL_OK;
 }
+
+int kpool_score_topk_noalloc_status(int *status_out)
+{
+    clear_error();
+    if (!status_out) return fail(KPOOL_ERR_INVALID_ARG, "NULL pointer");
+    int *scratch = nullptr;
+    size_t scratch_bytes = 0;
+    int64_t max_tiles = 0;
+    const int rc = noalloc_scratch(&scratch, &scratch_bytes, &max_tiles);
+    if (rc) return rc;
+    return kpool_read_status(scratch, status_out);
+}
+
+uint64_t kpool_debug_set_wait_limit_ns(uint64_t ns) { return set_wait_limit_ns(ns); }
 
 }  // extern "C"

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the library's translation units.
 #pragma once
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 #include <cstdio>
@@ -16,6 +17,16 @@ void clear_error();
 const char *last_error_cstr();
 
 int fail(int code, const char *fmt, ...);
+
+// NVTX range around one C ABI call (a no-op unless a profiler or tracer
+// injects an NVTX handler): nsys / ncu timelines show each entry point.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define KPOOL_NVTX_RANGE(name) ::kpool::NvtxRange kpool_nvtx_range_(name)
 
 // Number of SMs of the current device (cached per device).
 int num_sms();
@@ -72,6 +83,9 @@ size_t score_workspace_bytes(int64_t T, int H, int n_docs);
 // (equal to score_workspace_bytes when the call cannot use it).
 size_t score_workspace_split_bytes(int64_t T, int H, int n_docs, int Kp);
 int score_capacity(int H, int D, int fp8);   // candidate slots per query (0 = unsupported)
+// Limit of one scoring-pipeline wait for later launches (0 = the 2 s
+// default); returns the previous limit.
+uint64_t set_wait_limit_ns(uint64_t ns);
 int run_score(const ScoreArgs &a, cudaStream_t s);
 // Host-buffer pass with copies overlapped (kpool_pipeline.cu).  All input
 // pointers are host memory; cu_seqlens_host NULL means one sequence (n_docs =

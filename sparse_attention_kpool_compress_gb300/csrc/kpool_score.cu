@@ -27,6 +27,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 #include <cstring>
 #include <mutex>
@@ -47,7 +48,7 @@ constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
 constexpr int kSmemLimit = 232448;                    // 227 KiB per block (opt-in max)
 constexpr int kMaxC = 4096;
-constexpr uint64_t kTimeoutNs = 2000000000ull;        // 2 s per wait
+constexpr uint64_t kTimeoutNs = 2000000000ull;        // 2 s: default wait limit, drain bound
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kGroups = 4;                            // selection groups of the epilogue
 constexpr int kGroupWarps = kEpiWarps / kGroups;      // 4 warps per group
@@ -128,7 +129,7 @@ Layout make_layout(int H, int D, int fp8, int stages = 0)
     L.thr_off = off;  off += ((QT * 4 + 15) / 16) * 16;
     L.bar_off = off;  off += 256;
     L.ti_off = off;   off += 3 * 64;   // two producer slots + the epilogue's current unit
-    L.misc_off = off; off += 16;
+    L.misc_off = off; off += 32;   // tmem, abort, split flag, -, epilogue agreement [4]
     const int avail = kSmemLimit - 1024 - static_cast<int>(off);
     int C = avail / (8 * QT);
     C &= ~31;
@@ -159,6 +160,7 @@ struct Params {
     int32_t *part_idx;   // [slot][QT][Kp]
     float *part_score;   // [slot][QT][Kp]
     uint32_t q_tx, pk_tx, idesc;
+    uint64_t wait_limit_ns;   // limit of one pipeline wait (kTimeoutNs unless a test lowers it)
     Layout L;
 };
 
@@ -173,10 +175,12 @@ __device__ __forceinline__ uint32_t fkey(float f)
 struct Sync {
     volatile uint32_t *abort_flag;
     int *status;
+    uint64_t limit_ns;
 };
 
 // Bounded mbarrier wait: completion first, then the CTA abort flag, then a
-// 2 s timer (sets KPOOL_STATUS_TIMEOUT and the abort flag).
+// timer of limit_ns (sets KPOOL_STATUS_TIMEOUT and the abort flag).  Once the
+// abort flag is up every later wait returns after one probe.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sync &sy)
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -184,7 +188,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sy
     while (true) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*sy.abort_flag) return false;
-        if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        if (ptx::globaltimer() - t0 > sy.limit_ns) {
             *sy.abort_flag = 1u;
             atomicOr(sy.status, KPOOL_STATUS_TIMEOUT);
             return false;
@@ -651,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(BPK_FULL + S + s), 1);
         }
         misc[1] = 0u;
+        for (int i = 4; i < 8; ++i) misc[i] = 0u;
         int *qcnt0 = reinterpret_cast<int *>(smem + L.cnt_off);
         uint32_t *thr0 = reinterpret_cast<uint32_t *>(smem + L.thr_off);
         for (int q = 0; q < QT; ++q) {
@@ -667,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = misc[0];
-    Sync sy{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.ws + WS_STATUS};
+    Sync sy{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.ws + WS_STATUS, p.wait_limit_ns};
 
     auto tile_info = [&](int tile) {
         TileInfo t{};
@@ -908,17 +913,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0, tile_seq = 0;
         uint32_t acc_ph = 0;
         PT_DECL
+        // The 16 epilogue warps meet at named barriers, so they leave the tile
+        // loop only together: a warp whose wait fails (timeout or CTA abort)
+        // raises a per-iteration agreement word and keeps to the common control
+        // flow; every warp reads the word after the next barrier they all pass
+        // (the weight-staging barrier for the tile-info wait, the barrier before
+        // the final selection for the accumulator waits) and they all leave
+        // there.  Words alternate by iteration parity: a word is written only
+        // before its barrier and read only after it, and its next use is two
+        // iterations (several barriers) later.
         for (int it = 0;; ++it) {
             const int slot = it & 1;
             const uint32_t tph = (it >> 1) & 1;
+            volatile uint32_t *agree_ti = misc + 4 + slot;   // a tile-info wait failed
+            volatile uint32_t *agree_tm = misc + 6 + slot;   // an accumulator wait failed
             PT_MARK(7);
-            if (!wait_bar_warp(bar(BTI_FULL + slot), tph, sy)) break;
+            const bool ti_ok = wait_bar_warp(bar(BTI_FULL + slot), tph, sy);
             PT_MARK(0);
-            const TileInfo t = ti_slots[slot];
-            if (kFew && etid == 0) ti_slots[2] = t;   // for the unit's end (visible after the w barrier)
+            TileInfo t{};
+            t.t0 = -1;
+            if (ti_ok) t = ti_slots[slot];
+            if (kFew && etid == 0 && ti_ok) ti_slots[2] = t;   // for the unit's end (visible after the w barrier)
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(BTI_EMPTY + slot));
-            if (t.t0 < 0) break;
+            if (lane == 0) {
+                if (ti_ok) ptx::mbar_arrive(bar(BTI_EMPTY + slot));
+                else *agree_ti = 1u;
+            }
             const int tau0 = t.pos_base + (t.t0 - t.doc_start);
             const int nq = min(QT, t.doc_end - t.t0);
 
@@ -928,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (etid < kBN) {
                 const int qi = lone ? 0 : etid / H;
                 float v = 0.f;
-                if (qi < nq) {
+                if (t.t0 >= 0 && qi < nq) {
                     const int64_t off = static_cast<int64_t>(t.t0) * H + (lone ? etid % H : etid);
                     v = __ldg(p.w + off);
                     if (p.fp8) v *= __ldg(p.q_scale + off);
@@ -936,6 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wsm[etid] = v;
             }
             ptx::named_bar_sync(1, kEpiThreads);
+            if (*agree_ti != 0u || t.t0 < 0) break;   // the same outcome in every warp
 
             uint32_t thr[QS];
             int nc[QS];
@@ -952,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto tiles = [&]() {
             for (int i = 0; i < npt; ++i) {
                 PT_MARK(1);
-                if (!wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy)) { aborted = true; break; }
+                aborted |= !wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy);
                 PT_MARK(2);
                 ptx::tc_fence_after();
                 // relu(x) * w summed per query over this warp's 64 columns
@@ -1088,10 +1109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t thr0 = 0u;
                     for (int m = 0; m < nquad; ++m) {
                         PT_MARK(1);
-                        if (!wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy)) {
-                            aborted = true;
-                            break;
-                        }
+                        aborted |= !wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy);
                         PT_MARK(2);
                         ptx::tc_fence_after();
                         uint64_t a4[NACC];
@@ -1174,15 +1192,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 tiles();
             }
-            if (aborted) break;
-            if (p.mode == 1) {
-                ptx::named_bar_sync(1, kEpiThreads);   // w staging is rewritten next
-                continue;
-            }
+            // after an abort the loop ran on to the tile's end without waiting
+            // (its scores are garbage); all warps leave here together
+            if (aborted && lane == 0) *agree_tm = 1u;
+            PT_MARK(1);
+            ptx::named_bar_sync(1, kEpiThreads);   // also: w staging is rewritten next
+            if (*agree_tm != 0u) break;
+            if (p.mode == 1) continue;
 
             // final selection, pool order and output: every group on its own queries
-            PT_MARK(1);
-            ptx::named_bar_sync(1, kEpiThreads);
             bool emit = true;
             if constexpr (kFew) {
                 if (ti_slots[2].splits > 1)
@@ -1423,6 +1441,10 @@ __global__ void fill_kernel(uint32_t *a, int64_t n, uint32_t va, uint32_t *b, ui
 
 // ---- host side -------------------------------------------------------------
 
+// Limit of one pipeline wait, for every scoring launch of the process
+// (kpool_debug_set_wait_limit_ns; tests lower it to make waits expire).
+std::atomic<uint64_t> g_wait_limit_ns{kTimeoutNs};
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1578,6 +1600,11 @@ size_t score_workspace_split_bytes(int64_t T, int H, int n_docs, int Kp)
     return split_layout(T, H, n_docs, Kp).bytes;
 }
 
+uint64_t set_wait_limit_ns(uint64_t ns)
+{
+    return g_wait_limit_ns.exchange(ns == 0 ? kTimeoutNs : ns);
+}
+
 int score_capacity(int H, int D, int fp8)
 {
     const Layout L = make_layout(H, D, fp8);
@@ -1649,6 +1676,7 @@ int run_score(const ScoreArgs &a, cudaStream_t s)
     prm.q_tx = L.n_kchunks * L.q_chunk;
     prm.pk_tx = L.n_kchunks * L.pk_chunk;
     prm.idesc = ptx::make_idesc(a.fp8 ? 0u : 1u, kBM, kBN);
+    prm.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     prm.L = L;
 
     int grid;

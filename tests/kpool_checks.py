@@ -48,7 +48,8 @@ def check_pooled_keys(got_bits, want_bits, exact, cond, name=""):
 
 def check_selection(ora, ops, cu_seqlens, kp, Kp, rows, gpu_idx, gpu_score, tol, name=""):
     """rows: int64 array of query rows; gpu_idx/gpu_score: [len(rows), Kp]
-    numpy arrays of the GPU output for those rows.  Returns a dict of stats;
+    numpy arrays of the GPU output for those rows (gpu_score None: a path that
+    returns only indices; the set checks still run).  Returns a dict of stats;
     raises AssertionError on a violation."""
     rows = np.asarray(rows, dtype=np.int64)
     o = ora.select_rows(ops, cu_seqlens, kp, Kp, rows)
@@ -61,7 +62,9 @@ def check_selection(ora, ops, cu_seqlens, kp, Kp, rows, gpu_idx, gpu_score, tol,
         assert gv.size == ns, "%s row %d: %d selected, oracle %d" % (name, rows[i], gv.size, ns)
         assert np.all(g[ns:] == -1), "%s row %d: padding" % (name, rows[i])
         assert np.all(np.diff(gv) > 0), "%s row %d: not strictly ascending" % (name, rows[i])
-        assert np.all(np.isneginf(gpu_score[i][ns:])), "%s row %d: score padding" % (name, rows[i])
+        if gpu_score is not None:
+            assert np.all(np.isneginf(gpu_score[i][ns:])), "%s row %d: score padding" % (
+                name, rows[i])
         pair_r.extend([rows[i]] * ns)
         pair_p.extend(gv.tolist())
         ov = o["sel"][i][: ns]
@@ -82,6 +85,8 @@ def check_selection(ora, ops, cu_seqlens, kp, Kp, rows, gpu_idx, gpu_score, tol,
         for j, p in enumerate(g):
             s, c = lut[(r, int(p))]
             assert np.isfinite(s), "%s row %d: pool %d not causal" % (name, r, p)
+            if gpu_score is None:
+                continue
             err = abs(float(gpu_score[i][j]) - s)
             lim = tol * c + 1e-30
             max_rel = max(max_rel, err / (c + 1e-30))
@@ -110,3 +115,21 @@ def check_dense_scores(gpu, ora_scores, ora_cond, tol, name=""):
     assert not bad.any(), "%s: %d scores out of tolerance, worst %r" % (
         name, int(bad.sum()), float((err / (ora_cond[fin] + 1e-30)).max()))
     return float((err / (ora_cond[fin] + 1e-30)).max()) if err.size else 0.0
+
+
+def pools_from_tokens(tok, rows, cu_seqlens, T, kp, n_sel):
+    """Recover each row's pool list from its token row (the first n_sel * kp
+    entries are whole pools in ascending order): [len(rows), max n_sel]
+    global pool indices, -1 padded.  Checks that every group of kp tokens is
+    one aligned pool of the row's document."""
+    cu = np.asarray(cu_seqlens if cu_seqlens is not None else [0, T], np.int64)
+    cp = np.concatenate([[0], np.cumsum((cu[1:] - cu[:-1]) // kp)])
+    width = int(max(n_sel)) if len(n_sel) else 0
+    out = np.full((len(rows), max(width, 1)), -1, np.int64)
+    for i, t in enumerate(rows):
+        d = int(np.searchsorted(cu, t, side="right") - 1)
+        ns = int(n_sel[i])
+        grp = tok[i][: ns * kp].astype(np.int64).reshape(ns, kp) - cu[d]
+        assert np.all(grp[:, 0] % kp == 0) and np.all(grp - grp[:, :1] == np.arange(kp)), t
+        out[i, :ns] = cp[d] + grp[:, 0] // kp
+    return out

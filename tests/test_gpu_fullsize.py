@@ -7,7 +7,8 @@ oracle computes one by one: 1024 seeded rows plus the first and last 64
   The scorer is checked on the oracle's pooled keys (scores within
   1e-3 * S, selections equal up to near-tie swaps); the whole path
   (compress -> score/top-k -> expand) is checked for pooled keys, for the
-  structure of every row, and bit-exact expansion of the sampled rows.
+  structure of every row, for its own selection against the oracle's on
+  the sampled rows, and bit-exact expansion of the sampled rows.
 * fp8_2x32k: two sequences of 32768 tokens, E4M3 scoring.  End to end
   against the oracle's own FP8 chain with the FP8 tolerance 5e-2 * S.
 """
@@ -80,6 +81,13 @@ def test_long_128k(K, ora):
     assert st["swaps"] <= 4
     idx_h = idx.cpu().numpy()
     _row_structure(idx_h, T, kp, Kp, [0, T])
+    # the whole path's own selection (on the GPU's pooled keys) against the
+    # oracle's (on its pooled keys): pooled keys within 1 ulp move scores by far
+    # less than the near-tie band, so the sets agree up to near-tie swaps
+    st2 = check_selection(ora, ops, None, kp, Kp, rows, idx_h[rows], sc.cpu().numpy()[rows],
+                          TOL, "long_128k whole path")
+    print("long_128k whole path:", st2)
+    assert st2["swaps"] <= 8
     want = ora.expand_rows(idx_h[rows], None, T, kp, Kp, True, rows)
     assert np.array_equal(tok.cpu().numpy()[rows], want)
 
@@ -112,6 +120,9 @@ def test_fp8_2x32k(K, ora):
     ops = ora.Operands(qc, inp.w.numpy(), pc, qs, ps)
     st = check_selection(ora, ops, cu.numpy(), kp, Kp, rows, idx_h[rows], sc.cpu().numpy()[rows],
                          TOL_FP8, "fp8_2x32k")
-    assert st["swaps"] <= len(rows)
+    print("fp8_2x32k:", st)
+    # swaps come only from rows whose GPU E4M3 codes differ from the oracle's
+    # (the FP32 rotation landing next to a BF16 midpoint) or from near ties
+    assert st["swaps"] <= 64
     want = ora.expand_rows(idx_h[rows], cu.numpy(), T, kp, Kp, True, rows)
     assert np.array_equal(tok.cpu().numpy()[rows], want)

@@ -1,12 +1,15 @@
 """kpool_indexer_forward_host (host buffers in, host token indices out, copies
 overlapped with the kernels over query chunks) against the device path
 kpool_indexer_forward on the same inputs: identical token indices, bit for
-bit, for chunk sizes that cut through query tiles and documents."""
+bit, for chunk sizes that cut through query tiles and documents; and against
+the CPU oracle on sampled rows (selected pool sets equal up to near-tie
+swaps, token rows bit-exact given the pools)."""
 import numpy as np
 import pytest
 import torch
 
 from sparse_attention_kpool_compress_gb300 import workloads as W
+from kpool_checks import check_selection, pools_from_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -98,3 +101,30 @@ def test_two_queries_per_warp_packed(K):
                     doc_len_range=(800, 4000))
     inp = W.make_inputs(wl, seed=37)
     assert torch.equal(_host_tokens(K, inp, wl, False, 999), _device_tokens(K, inp, wl, False))
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_host_pass_matches_oracle(K, ora, packed):
+    """The host-buffer pass's token rows against the oracle on 256 sampled rows
+    (plus the first and last 16): the pools the rows hold are the oracle's
+    selection up to near-tie swaps (1e-3 * S of the Kp-th score), and each row
+    is the oracle's expansion of those pools plus the causal tail."""
+    if packed:
+        wl = W.Workload("o2", T=12000, H=64, D=128, kpool=4, index_topk=512, n_docs=6,
+                        doc_len_range=(300, 4000))
+    else:
+        wl = W.Workload("o1", T=16384, H=64, D=128, kpool=4, index_topk=512)
+    inp = W.make_inputs(wl, seed=41 + int(packed))
+    tok = _host_tokens(K, inp, wl, False, 3000).numpy()
+    cu = inp.cu_seqlens.numpy() if packed else None
+    rows = W.sample_rows(wl.T, n_sample=256, edge=16).numpy()
+    pkb = ora.compress(W.bits(inp.k), W.bits(inp.gate), inp.ape.numpy(), cu, wl.kpool)
+    ops = ora.Operands(W.bits(inp.q), inp.w.numpy(), pkb)
+    o = ora.select_rows(ops, cu, wl.kpool, wl.Kp, rows)
+    pools = pools_from_tokens(tok[rows], rows, cu, wl.T, wl.kpool, o["n_sel"])
+    idx = np.full((len(rows), wl.Kp), -1, np.int32)
+    idx[:, : pools.shape[1]] = pools
+    st = check_selection(ora, ops, cu, wl.kpool, wl.Kp, rows, idx, None, 1e-3, wl.name)
+    assert st["swaps"] <= 4, st
+    want = ora.expand_rows(idx, cu, wl.T, wl.kpool, wl.Kp, wl.tail, rows)
+    assert np.array_equal(tok[rows], want)
