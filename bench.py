@@ -422,6 +422,9 @@ def main():
     ap.add_argument("--e2e-chunk-rows", type=int, default=0,
                     help="query rows per chunk of the end-to-end pass (0 = the library's default)")
     ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--replicas", action="store_true",
+                    help="N > 1: every rank runs the whole workload (weak scaling) instead of "
+                         "scoring its share of the query rows (strong scaling)")
     ap.add_argument("--no-fp8-peak", action="store_true",
                     help="FP8 workloads: skip measuring the E4M3 peak (profiling runs); the "
                          "roofline then uses 2 x the BF16 burst peak, and says so")
@@ -449,6 +452,8 @@ def main():
     inp = W.make_inputs(wl)
     if wl.queries != "all":
         return run_positioned(args, wl, inp, K, dev, world, rank, local)
+    if world > 1 and not args.replicas:
+        return run_sharded(args, wl, inp, dev, world, rank, local)
     T, H, D, kp, topk, Kp = wl.T, wl.H, wl.D, wl.kpool, wl.index_topk, wl.Kp
     multi = inp.cu_seqlens.numel() > 2
     if multi:
@@ -851,6 +856,100 @@ def run_positioned(args, wl, inp, K, dev, world, rank, local):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_sharded(args, wl, inp, dev, world, rank, local):
+    """N > 1 ranks share one workload (strong scaling): each holds the rows of
+    its shard (zigzag blocks of one sequence, or whole packed documents) and
+    runs the query-sharded pass (sparse_attention_kpool_compress_gb300.sharding);
+    one sequence exchanges pooled keys with an NCCL all-gather.  A step is one
+    whole pass of every rank; its time is the max over ranks, and the job
+    processes the workload's T queries per step."""
+    import torch.distributed as dist
+    from sparse_attention_kpool_compress_gb300 import sharding as S
+    cu = inp.cu_seqlens.tolist() if inp.cu_seqlens.numel() > 2 else None
+    plan = S.plan_shards(wl.T, world, rank, wl.kpool, cu)
+    q, k, gate, w = (S.shard_rows(x, plan).to(dev) for x in (inp.q, inp.k, inp.gate, inp.w))
+    ape = inp.ape.to(dev)
+    idx = S.ShardedIndexer(plan, wl.index_topk, wl.tail, wl.fp8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        idx.forward(q, k, gate, ape, w)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def barrier():
+        dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    in_bytes = sum(x.numel() * x.element_size() for x in (q, k, gate, w))
+    ms_step, _, clocks, _ = timed_loop(step, 1, args.steps, stream, in_bytes, local, barrier)
+    ms_step = job_time_ms(ms_step, world, dev)
+
+    e2e = None
+    if not args.no_e2e:
+        hsrc = [x.cpu().pin_memory() for x in (q, k, gate, w)]
+        dsts = [torch.empty_like(x) for x in (q, k, gate, w)]
+        Wd = wl.Kp * wl.kpool + wl.kpool - 1
+        htok = torch.empty(plan.local_rows, Wd, dtype=torch.int32).pin_memory()
+
+        def e2e_step():
+            for d_, h_ in zip(dsts, hsrc):
+                d_.copy_(h_, non_blocking=True)
+            tok = idx.forward(dsts[0], dsts[1], dsts[2], ape, dsts[3])
+            htok.copy_(tok, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(2, min(args.steps, 5))
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = job_time_ms(a0.elapsed_time(a1) / n_e2e, world, dev)
+        e2e = {"value": wl.T / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
+               "steps": n_e2e, "h2d_bytes_per_step": sum(x.numel() * x.element_size()
+                                                          for x in hsrc),
+               "d2h_bytes_per_step": htok.numel() * 4,
+               "api": "ShardedIndexer.forward per rank (rank 0's bytes)"}
+
+    peaks, peak_src = load_peaks()
+    flops = 2.0 * wl.H * wl.D * sum_floor_pairs(inp.cu_seqlens, wl.kpool)
+    tflops = flops / (ms_step / 1000.0) / 1e12
+    peak = peaks["bf16_tflops"] * (2 if wl.fp8 else 1) * world
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": wl.T / (ms_step / 1000.0), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+            "dtype": "fp8-e4m3" if wl.fp8 else "bf16", "data": "synthetic",
+            "config": dict(bench_config(wl, inp, 1),
+                           parallelism="%s-%d" % (plan.layout, world)),
+            "scoring_tflops": tflops, "e2e": e2e,
+            # rank 0's own kernels: compress, [FP8 q cast], and per scoring call
+            # the schedule, scoring and expansion kernels
+            "gpu_launches": args.steps * (1 + int(wl.fp8) + 3 * (
+                len(plan.segments) if plan.layout == "zigzag" else int(bool(plan.segments)))),
+            "roofline": {"bound": "tensor", "kernel": "whole sharded step", "achieved": tflops,
+                         "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "traffic": None,
+                         "peak_source": "%d x %s burst (%s)" % (world, "2 x bf16" if wl.fp8
+                                                                else "bf16", peak_src)},
+            "cpu_baseline": None, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
     return 0
 
 
