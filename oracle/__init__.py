@@ -23,6 +23,10 @@ What each function follows (page titles and sections):
   ``index_topk // kpool`` selection, ties to the lower pool index.
 * ``expand_rows`` -- expansion of pools to tokens plus the causal tail
   (``always_select_tail``).
+* ``project_keys`` -- the key path in front of compression: Megatron-LM PR
+  Changes section 4 (linear_wk and k_norm in BF16, unquantized) and section
+  3 / SkyRL commit "k-pool indexer" (the BF16 compression gate); k_norm is
+  read as a LayerNorm with weight and bias.
 
 Every function is pinned by ``tests/test_oracle_pins.py``; none is left
 unpinned.
@@ -74,6 +78,8 @@ def _load():
             "ora_cu_pools": (i64, [P, i32, i32, P]),
             "ora_compress": (None, [P, P, P, P, i32, i32, i32, P, P, P]),
             "ora_pool_weights": (None, [P, P, i64, i32, i32, P]),
+            "ora_project_keys": (None, [P, P, P, P, ctypes.c_double, i64, i32, i32, P, P, P, P,
+                                        P]),
             "ora_hadamard_matrix": (None, [i32, P]),
             "ora_fp8_rows": (None, [P, i64, i32, P, P, P, P]),
             "ora_score_pairs": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i64,
@@ -172,6 +178,26 @@ def compress(k_bits, gate_bits, ape, cu_seqlens, kp: int, want_exact: bool = Fal
     if want_cond:
         return pk, exact, cond
     return (pk, exact) if want_exact else pk
+
+
+def project_keys(x_bits, w_bits, gamma, beta, eps: float, want_exact: bool = False):
+    """The key path in front of compression: x_bits bf16 [T, hidden], w_bits
+    bf16 [2D, hidden] (W_k rows then the gate projection's rows), gamma and
+    beta float32 [D].  Returns (k bits, gate bits) uint16 [T, D]; with
+    want_exact also the unrounded (kproj, k, gate) doubles."""
+    x_bits = _c(x_bits, np.uint16)
+    w_bits = _c(w_bits, np.uint16)
+    gamma = _c(gamma, np.float32)
+    beta = _c(beta, np.float32)
+    T, hidden = x_bits.shape
+    D = w_bits.shape[0] // 2
+    assert w_bits.shape == (2 * D, hidden) and D <= 256 and gamma.shape == beta.shape == (D,)
+    k = np.empty((T, D), np.uint16)
+    g = np.empty((T, D), np.uint16)
+    ex = [np.empty((T, D), np.float64) for _ in range(3)] if want_exact else [None] * 3
+    _load().ora_project_keys(_ptr(x_bits), _ptr(w_bits), _ptr(gamma), _ptr(beta), float(eps), T,
+                             hidden, D, _ptr(k), _ptr(g), _ptr(ex[0]), _ptr(ex[1]), _ptr(ex[2]))
+    return (k, g, ex[0], ex[1], ex[2]) if want_exact else (k, g)
 
 
 def pool_weights(gate_bits, ape, first_token: int, kp: int) -> np.ndarray:

@@ -223,6 +223,53 @@ void ora_compress(const uint16_t *k, const uint16_t *gate, const float *ape,
     free(cu_pools);
 }
 
+/* The key path in front of compression (Megatron-LM PR, Changes section 4:
+ * linear_wk and k_norm run unquantized, in BF16; section 3 and the SkyRL
+ * commit "k-pool indexer": the BF16 per-token compression gate).  For every
+ * token t, with W = [W_k; W_g] of shape [2D, hidden] (rows are output
+ * features, as a linear layer's weight):
+ *   kproj[t, j] = bf16_rne( sum_i x[t, i] * W[j, i] )          j < D
+ *   gate[t, j]  = bf16_rne( sum_i x[t, i] * W[D + j, i] )      j < D
+ *   mu = mean_j kproj[t, j],  var = mean_j (kproj[t, j] - mu)^2
+ *   k[t, j]     = bf16_rne( (kproj[t, j] - mu) / sqrt(var + eps) * gamma[j] + beta[j] )
+ * (k_norm read as a LayerNorm with weight and bias, biased variance), each
+ * formed in double and rounded once.  The exact (unrounded) values are
+ * returned when the pointers are non-NULL. */
+void ora_project_keys(const uint16_t *x, const uint16_t *w, const float *gamma,
+                      const float *beta, double eps, int64_t T, int hidden, int D,
+                      uint16_t *k_out, uint16_t *gate_out, double *kproj_exact,
+                      double *k_exact, double *gate_exact)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++) {
+        double kp[512];
+        double mu = 0.0;
+        for (int j = 0; j < 2 * D; j++) {
+            double acc = 0.0;
+            for (int i = 0; i < hidden; i++)
+                acc += ora_bf16_to_double(x[t * hidden + i]) * ora_bf16_to_double(w[(int64_t)j * hidden + i]);
+            if (j < D) {
+                if (kproj_exact) kproj_exact[t * D + j] = acc;
+                kp[j] = ora_bf16_to_double(ora_bf16_from_double(acc));
+                mu += kp[j];
+            } else {
+                if (gate_exact) gate_exact[t * D + j - D] = acc;
+                gate_out[t * D + j - D] = ora_bf16_from_double(acc);
+            }
+        }
+        mu /= D;
+        double var = 0.0;
+        for (int j = 0; j < D; j++) var += (kp[j] - mu) * (kp[j] - mu);
+        var /= D;
+        const double rs = 1.0 / sqrt(var + eps);
+        for (int j = 0; j < D; j++) {
+            const double v = (kp[j] - mu) * rs * (double)gamma[j] + (double)beta[j];
+            if (k_exact) k_exact[t * D + j] = v;
+            k_out[t * D + j] = ora_bf16_from_double(v);
+        }
+    }
+}
+
 /* Softmax weights of one pool (for the sum-to-one pin). */
 void ora_pool_weights(const uint16_t *gate, const float *ape, int64_t first_token,
                       int D, int kp, double *alpha /* [kp, D] */)

@@ -683,3 +683,71 @@ def test_compress_hand_worked_moderate_logits(ora, kp):
     pk = ora.compress(W.bits(kb), W.bits(gb), ape, None, kp)
     assert pk.shape == (1, 32)
     assert np.array_equal(bf16_val(pk[0]), want), (bf16_val(pk[0]), want)
+
+
+# ---------------------------------------------------------------------------
+# The key path in front of compression (linear_wk -> k_norm, gate projection)
+# ---------------------------------------------------------------------------
+
+def _nearest_bf16(bits, exact):
+    """Each BF16 value is within half a BF16 spacing of its exact value (8
+    significant bits: spacing 2^(floor(log2|v|) - 7))."""
+    v = bf16_val(bits)
+    nz = exact != 0
+    e = np.floor(np.log2(np.abs(np.where(nz, exact, 1.0))))
+    half = 2.0 ** (e - 8)
+    return bool(np.all(np.abs(v - exact)[nz] <= half[nz]) and np.all(v[~nz] == 0))
+
+
+def _proj_inputs(T=24, hidden=96, D=32, seed=12):
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, hidden, generator=gen).to(torch.bfloat16)
+    w = (torch.randn(2 * D, hidden, generator=gen) / math.sqrt(hidden)).to(torch.bfloat16)
+    gamma = (1.0 + 0.1 * torch.randn(D, generator=gen)).float()
+    beta = (0.1 * torch.randn(D, generator=gen)).float()
+    return x, w, gamma, beta
+
+
+def test_project_keys_is_a_matmul_then_layer_norm(ora):
+    """The projections equal numpy's float64 matmul of the BF16 operands (the
+    first D weight rows give the keys, the next D the gate), and the key
+    normalisation equals torch's float64 layer_norm (biased variance, eps
+    inside the square root, weight and bias) of the BF16-rounded projection."""
+    x, w, gamma, beta = _proj_inputs()
+    eps = 1e-6
+    k, g, kp_ex, k_ex, g_ex = ora.project_keys(W.bits(x), W.bits(w), gamma.numpy(), beta.numpy(),
+                                               eps, want_exact=True)
+    xd, wd = x.double().numpy(), w.double().numpy()
+    D = w.shape[0] // 2
+    assert np.allclose(kp_ex, xd @ wd[:D].T, rtol=1e-12, atol=1e-13)
+    assert np.allclose(g_ex, xd @ wd[D:].T, rtol=1e-12, atol=1e-13)
+    assert _nearest_bf16(g, g_ex)
+    kp_r = bf16_val(bf16_bits_of(kp_ex.astype(np.float32)))
+    ln = torch.nn.functional.layer_norm(torch.from_numpy(kp_r), (D,),
+                                        gamma.double(), beta.double(), eps).numpy()
+    assert np.allclose(k_ex, ln, rtol=1e-10, atol=1e-12)
+    assert _nearest_bf16(k, k_ex)
+
+
+def test_project_keys_closed_forms(ora):
+    """A zero input row normalises to the bias exactly; a projection that takes
+    only the values +a and -a in equal numbers normalises to
+    +-a / sqrt(a^2 + eps) * gamma + beta."""
+    T, hidden, D = 3, 64, 32
+    x = torch.zeros(T, hidden)
+    x[1, 0] = 1.0
+    x[2, 0] = 0.5
+    w = torch.zeros(2 * D, hidden)
+    w[:D, 0] = torch.tensor([2.0, -2.0] * (D // 2))      # kproj = +-2 x[:, 0]
+    w[D:, 1] = 1.0
+    gamma = torch.linspace(0.5, 1.5, D)
+    beta = torch.linspace(-0.25, 0.25, D)
+    eps = 1e-6
+    k, g, _, k_ex, _ = ora.project_keys(W.bits(x.to(torch.bfloat16)), W.bits(w.to(torch.bfloat16)),
+                                        gamma.numpy(), beta.numpy(), eps, want_exact=True)
+    assert np.array_equal(k_ex[0], beta.double().numpy())
+    for t, a in ((1, 2.0), (2, 1.0)):
+        sign = np.array([1.0, -1.0] * (D // 2))
+        want = sign * a / math.sqrt(a * a + eps) * gamma.double().numpy() + beta.double().numpy()
+        assert np.allclose(k_ex[t], want, rtol=1e-14, atol=1e-15)
+    assert not np.any(bf16_val(g))     # the gate column of x is zero
