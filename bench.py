@@ -23,6 +23,7 @@ no exchange step); time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -415,7 +416,8 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="long_128k", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="long_128k",
+                    choices=sorted(W.WORKLOADS) + sorted(W.PROJECTION_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--baseline-rows", type=int, default=3584)
@@ -434,6 +436,8 @@ def main():
     if args.warmup < 3:
         print("warmup raised to 3 (minimum)", file=sys.stderr)
         args.warmup = 3
+    if args.workload in W.PROJECTION_WORKLOADS:
+        return run_projection(args)
     wl = W.WORKLOADS[args.workload]
     if args.T is not None:
         from dataclasses import replace
@@ -950,6 +954,97 @@ def run_sharded(args, wl, inp, dev, world, rank, local):
         }
         print(json.dumps(line), flush=True)
     dist.destroy_process_group()
+    return 0
+
+
+def run_projection(args):
+    """The key path fused with compression (kpool_project_compress): hidden
+    states to pooled keys in one kernel.  HBM-bound (the hidden states are read
+    once); the roofline counts x, the weights and the pooled keys written."""
+    cfg = dict(W.PROJECTION_WORKLOADS[args.workload])
+    if args.T is not None:
+        cfg["T"] = args.T
+    T, hidden, D, kp = cfg["T"], cfg["hidden"], cfg["D"], cfg["kpool"]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm covers the indexer "
+                          "workloads; the projection has no CPU baseline line"}), flush=True)
+        return 0
+    torch.cuda.set_device(local)
+    import sparse_attention_kpool_compress_gb300 as K
+    dev = torch.device("cuda", local)
+    pi = W.make_projection_inputs(T, hidden, D, kp)
+    x, w = pi.x.to(dev), pi.w_kg.to(dev)
+    gamma, beta, ape = pi.gamma.to(dev), pi.beta.to(dev), pi.ape.to(dev)
+    P = T // kp
+    pk = torch.empty(P, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    B = K.binding
+    L = B._lib
+    sp = B._stream(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        rc = L.kpool_project_compress(B._ptr(x), B._ptr(w), B._ptr(gamma), B._ptr(beta),
+                                      ctypes.c_float(pi.eps), B._ptr(ape), None, None, 1, T,
+                                      hidden, D, kp, P, B._ptr(pk), None, None, B._ptr(ws),
+                                      ws.numel(), sp)
+        if rc != 0:
+            raise B.KPoolError(rc, "kpool_project_compress")
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if K.kpool_read_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    in_bytes = x.numel() * 2 + w.numel() * 2
+    ms, _, clocks, l2_note = timed_loop(step, 1, args.steps, stream, in_bytes, local,
+                                        lambda: None)
+    peaks, peak_src = load_peaks()
+    alg = T * hidden * 2 + 2 * D * hidden * 2 + P * D * 2
+    gbs = alg / (ms / 1000.0) / 1e9
+    flops = 2.0 * T * hidden * 2 * D
+    e2e = None
+    if not args.no_e2e:
+        hx = pi.x.pin_memory()
+        hpk = torch.empty(P, D, dtype=torch.bfloat16).pin_memory()
+        xd = torch.empty_like(x)
+
+        def e2e_step():
+            xd.copy_(hx, non_blocking=True)
+            K.kpool_project_compress(xd, w, gamma, beta, pi.eps, ape, kp, workspace=ws)
+            hpk.copy_(pk, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(5):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        me = a0.elapsed_time(a1) / 5
+        e2e = {"value": T / (me / 1000.0), "unit": "tokens/s", "ms_per_step": me, "steps": 5,
+               "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hpk.numel() * 2}
+    line = {
+        "metric": "KPool key path fused with compression, tokens/s", "value": T / (ms / 1000.0),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": cfg["desc"], "T": T, "hidden": hidden,
+                   "D": D, "kpool": kp, "parallelism": "single", "l2": l2_note},
+        "e2e": e2e, "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "kernel": "kpool_project_compress", "achieved": gbs,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": "hbm copy (%s)" % peak_src,
+                     "algorithmic_bytes_per_launch": alg, "tensor_tflops": flops / ms / 1e9},
+        "cpu_baseline": None, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 

@@ -120,6 +120,40 @@ KPOOL_API int kpool_compress(const void *k, const void *gate, const float *ape,
                    uint8_t *pk_fp8_out, float *pk_scale_out, kpool_stream_t stream);
 
 /*
+ * kpool_project_compress -- the key path in front of compression fused with
+ * it (Megatron-LM PR section 4: linear_wk and k_norm run unquantized in BF16;
+ * section 3 and SkyRL commit "k-pool indexer": the BF16 per-token compression
+ * gate, then the pooling of kpool_compress).  For every token t:
+ *     kproj[t, :] = bf16_rne( x[t, :] . w_kg[0:D, :]^T )      (FP32 accumulation)
+ *     gate[t, :]  = bf16_rne( x[t, :] . w_kg[D:2D, :]^T )
+ *     k[t, :]     = bf16_rne( (kproj - mean) / sqrt(var + eps) * k_norm_weight
+ *                             + k_norm_bias )                  (LayerNorm, FP32,
+ *                                                               biased variance)
+ * and pk is kpool_compress(k, gate, ape) -- bit for bit the same pooled keys.
+ * The projected keys and gate are written only if k_out / gate_out are given.
+ *   x            bf16 [T, hidden] hidden states, 16-byte aligned
+ *   w_kg         bf16 [2D, hidden]: rows 0..D-1 the key projection, rows
+ *                D..2D-1 the gate projection (a linear layer's weight layout)
+ *   k_norm_weight, k_norm_bias   fp32 [D]
+ *   ape, cu_seqlens, cu_pools, n_docs, T, P_total, pk_out   as kpool_compress
+ *   k_out, gate_out   NULL or bf16 [T, D]
+ *   workspace    >= 256 bytes, 256-byte aligned: its status word
+ *                (kpool_read_status) reports a pipeline timeout
+ * Supported: D = 128; hidden a multiple of 64; kpool in {1, 2, 4, 8, 16, 32}.
+ * For FP8 pooled keys pass pk_out through kpool_quantize_fp8 (the same codes
+ * kpool_compress's FP8 outputs hold).  The head-weight projection (FP32) and
+ * the query projection are not part of this call.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE.
+ */
+KPOOL_API int kpool_project_compress(const void *x, const void *w_kg, const float *k_norm_weight,
+                                     const float *k_norm_bias, float k_norm_eps, const float *ape,
+                                     const int32_t *cu_seqlens, const int32_t *cu_pools,
+                                     int n_docs, int64_t T, int hidden, int D, int kpool,
+                                     int64_t P_total, void *pk_out, void *k_out, void *gate_out,
+                                     void *workspace, size_t workspace_bytes,
+                                     kpool_stream_t stream);
+
+/*
  * kpool_quantize_fp8 -- FP8 indexer input emulation (Megatron-LM PR
  * section 3: FP32 Hadamard -> BF16 -> E4M3 with a power-of-two row scale).
  * For each row r of x (bf16 [rows, 128]):

@@ -23,6 +23,10 @@ What each function follows (page titles and sections):
   ``index_topk // kpool`` selection, ties to the lower pool index.
 * ``expand_rows`` -- expansion of pools to tokens plus the causal tail
   (``always_select_tail``).
+* ``sparse_attn`` -- the sparse attention that consumes the selection:
+  xtuner PR "GLM-5.3-Flash F5: NoPE DSA + KPool indexer", Summary (NoPE
+  sparse MLA, FlashMLA-style forward) and Megatron-LM PR section 3 (NoPE:
+  no rotary slice); absorbed form, keys and values are the latent rows.
 * ``project_keys`` -- the key path in front of compression: Megatron-LM PR
   Changes section 4 (linear_wk and k_norm in BF16, unquantized) and section
   3 / SkyRL commit "k-pool indexer" (the BF16 compression gate); k_norm is
@@ -79,7 +83,7 @@ def _load():
             "ora_compress": (None, [P, P, P, P, i32, i32, i32, P, P, P]),
             "ora_pool_weights": (None, [P, P, i64, i32, i32, P]),
             "ora_project_keys": (None, [P, P, P, P, ctypes.c_double, i64, i32, i32, P, P, P, P,
-                                        P]),
+                                        P, P]),
             "ora_hadamard_matrix": (None, [i32, P]),
             "ora_fp8_rows": (None, [P, i64, i32, P, P, P, P]),
             "ora_score_pairs": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i64,
@@ -95,6 +99,7 @@ def _load():
                                           i32, P, i64, P, P, P, P, P]),
             "ora_expand_rows_at": (None, [P, P, P, P, i32, i32, i32, i32, P, i64, P]),
             "ora_num_threads": (i32, []),
+            "ora_sparse_attn": (None, [P, P, P, i32, i32, i32, ctypes.c_double, P, i64, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -184,7 +189,8 @@ def project_keys(x_bits, w_bits, gamma, beta, eps: float, want_exact: bool = Fal
     """The key path in front of compression: x_bits bf16 [T, hidden], w_bits
     bf16 [2D, hidden] (W_k rows then the gate projection's rows), gamma and
     beta float32 [D].  Returns (k bits, gate bits) uint16 [T, D]; with
-    want_exact also the unrounded (kproj, k, gate) doubles."""
+    want_exact also the unrounded (kproj, k, gate) doubles and the condition
+    scale of each normalised key."""
     x_bits = _c(x_bits, np.uint16)
     w_bits = _c(w_bits, np.uint16)
     gamma = _c(gamma, np.float32)
@@ -194,10 +200,11 @@ def project_keys(x_bits, w_bits, gamma, beta, eps: float, want_exact: bool = Fal
     assert w_bits.shape == (2 * D, hidden) and D <= 256 and gamma.shape == beta.shape == (D,)
     k = np.empty((T, D), np.uint16)
     g = np.empty((T, D), np.uint16)
-    ex = [np.empty((T, D), np.float64) for _ in range(3)] if want_exact else [None] * 3
+    ex = [np.empty((T, D), np.float64) for _ in range(4)] if want_exact else [None] * 4
     _load().ora_project_keys(_ptr(x_bits), _ptr(w_bits), _ptr(gamma), _ptr(beta), float(eps), T,
-                             hidden, D, _ptr(k), _ptr(g), _ptr(ex[0]), _ptr(ex[1]), _ptr(ex[2]))
-    return (k, g, ex[0], ex[1], ex[2]) if want_exact else (k, g)
+                             hidden, D, _ptr(k), _ptr(g), _ptr(ex[0]), _ptr(ex[1]), _ptr(ex[2]),
+                             _ptr(ex[3]))
+    return (k, g, ex[0], ex[1], ex[2], ex[3]) if want_exact else (k, g)
 
 
 def pool_weights(gate_bits, ape, first_token: int, kp: int) -> np.ndarray:
@@ -341,3 +348,22 @@ def expand_rows_at(sel, cu_q, q_pos, cu_k, kp: int, Kp: int, tail: bool, rows):
     _load().ora_expand_rows_at(_ptr(sel), _ptr(cq), _ptr(qp), _ptr(ck), len(cq) - 1, kp, Kp,
                                int(bool(tail)), _ptr(rows), n, _ptr(out))
     return out
+
+
+def sparse_attn(q_bits, c_bits, tok, scale: float, rows):
+    """Sparse attention over the selected tokens (absorbed NoPE form: keys and
+    values are the latent rows c).  q_bits bf16 [T, H, Dc], c_bits bf16 [Tk,
+    Dc], tok int32 [len(rows), W] token indices (-1 = none) for the query rows
+    `rows`.  Returns (o float64 [len(rows), H, Dc], lse float64 [len(rows), H])."""
+    q_bits = _c(q_bits, np.uint16)
+    c_bits = _c(c_bits, np.uint16)
+    tok = _c(tok, np.int32)
+    rows = _c(rows, np.int64)
+    T, H, Dc = q_bits.shape
+    n, W = tok.shape
+    assert n == len(rows) and c_bits.shape[1] == Dc
+    o = np.empty((n, H, Dc), np.float64)
+    lse = np.empty((n, H), np.float64)
+    _load().ora_sparse_attn(_ptr(q_bits), _ptr(c_bits), _ptr(tok), W, H, Dc, float(scale),
+                            _ptr(rows), n, _ptr(o), _ptr(lse))
+    return o, lse

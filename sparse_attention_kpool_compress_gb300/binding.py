@@ -42,6 +42,8 @@ _SIGS = {
     "kpool_cu_pools": (_I, [_P, _I, _I, _P, _P]),
     "kpool_compress": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _L, _P, _P, _P, _P]),
     "kpool_quantize_fp8": (_I, [_P, _L, _I, _P, _P, _P]),
+    "kpool_project_compress": (_I, [_P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _L, _I, _I,
+                                    _I, _L, _P, _P, _P, _P, _SZ, _P]),
     "kpool_score_topk_workspace_size": (_SZ, [_L, _I, _I]),
     "kpool_score_topk_workspace_size_split": (_SZ, [_L, _I, _I, _I, _I]),
     "kpool_score_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I, _I,
@@ -165,6 +167,39 @@ def kpool_compress(k, gate, ape, kpool: int, cu_seqlens=None, cu_pools=None, P_t
                                n_docs, T, D, kpool, P_total, _ptr(pk), _ptr(pk8), _ptr(sc),
                                _stream(k.device)), "kpool_compress")
     return (pk, pk8, sc) if fp8 else pk
+
+
+def kpool_project_compress(x, w_kg, k_norm_weight, k_norm_bias, k_norm_eps: float, ape,
+                           kpool: int, cu_seqlens=None, cu_pools=None, P_total=None,
+                           want_k_gate: bool = False, workspace=None):
+    """Pooled keys pk [P_total, 128] bf16 straight from hidden states x [T,
+    hidden] (key projection, k_norm, gate projection and compression in one
+    kernel); with want_k_gate also the projected keys and gate [T, 128]."""
+    _need(x, "x", torch.bfloat16)
+    _need(w_kg, "w_kg", torch.bfloat16)
+    for t_, n_ in ((k_norm_weight, "k_norm_weight"), (k_norm_bias, "k_norm_bias"), (ape, "ape")):
+        _need(t_, n_, torch.float32)
+    n_docs = _docs(cu_seqlens, cu_pools)
+    T, hidden = x.shape
+    D = w_kg.shape[0] // 2
+    if P_total is None:
+        if cu_seqlens is not None:
+            raise ValueError("P_total is required with cu_seqlens")
+        P_total = T // kpool
+    pk = torch.empty(P_total, D, dtype=torch.bfloat16, device=x.device)
+    k_out = g_out = None
+    if want_k_gate:
+        k_out = torch.empty(T, D, dtype=torch.bfloat16, device=x.device)
+        g_out = torch.empty(T, D, dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=x.device)
+    _check(_lib.kpool_project_compress(_ptr(x), _ptr(w_kg), _ptr(k_norm_weight),
+                                       _ptr(k_norm_bias), float(k_norm_eps), _ptr(ape),
+                                       _ptr(cu_seqlens), _ptr(cu_pools), n_docs, T, hidden, D,
+                                       kpool, P_total, _ptr(pk), _ptr(k_out), _ptr(g_out),
+                                       _ptr(workspace), workspace.numel(), _stream(x.device)),
+           "kpool_project_compress")
+    return (pk, k_out, g_out) if want_k_gate else pk
 
 
 def kpool_quantize_fp8(x):

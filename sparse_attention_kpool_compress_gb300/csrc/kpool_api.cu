@@ -533,6 +533,47 @@ int kpool_read_status(const void *workspace, int *status_out)
     return KPOOL_OK;
 }
 
+int kpool_project_compress(const void *x, const void *w_kg, const float *k_norm_weight,
+                           const float *k_norm_bias, float k_norm_eps, const float *ape,
+                           const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs,
+                           int64_t T, int hidden, int D, int kpool, int64_t P_total, void *pk_out,
+                           void *k_out, void *gate_out, void *workspace, size_t workspace_bytes,
+                           kpool_stream_t stream)
+{
+    clear_error();
+    KPOOL_NVTX_RANGE("kpool_project_compress");
+    int rc = check_common(T, kpool);
+    if (rc) return rc;
+    if (D != 128) return fail(KPOOL_ERR_UNSUPPORTED, "the fused projection needs D = 128 (got %d)", D);
+    if (32 % kpool != 0)
+        return fail(KPOOL_ERR_UNSUPPORTED, "the fused projection needs kpool dividing 32 (got %d)",
+                    kpool);
+    if (hidden < 64 || hidden % 64 != 0 || hidden > 65536)
+        return fail(KPOOL_ERR_UNSUPPORTED, "hidden must be a multiple of 64 in [64, 65536] (got %d)",
+                    hidden);
+    if (T * static_cast<int64_t>(hidden) > (int64_t(1) << 40))
+        return fail(KPOOL_ERR_UNSUPPORTED, "T * hidden too large");
+    if (P_total < 0) return fail(KPOOL_ERR_INVALID_ARG, "P_total < 0");
+    if ((rc = check_docs(cu_seqlens, cu_pools, n_docs, T, kpool, P_total))) return rc;
+    if (T > 0 && (!x || !w_kg || !k_norm_weight || !k_norm_bias || !ape))
+        return fail(KPOOL_ERR_INVALID_ARG, "x, w_kg, k_norm_weight, k_norm_bias and ape are required");
+    if (P_total > 0 && !pk_out) return fail(KPOOL_ERR_INVALID_ARG, "pk_out is required");
+    if (!aligned(x, 16) || !aligned(w_kg, 16) || !aligned(pk_out, 16) || !aligned(k_out, 16) ||
+        !aligned(gate_out, 16) || !aligned(ape, 4) || !aligned(k_norm_weight, 4) ||
+        !aligned(k_norm_bias, 4))
+        return fail(KPOOL_ERR_INVALID_ARG, "x, w_kg, pk_out, k_out and gate_out must be 16-byte aligned");
+    if (!(k_norm_eps >= 0.f)) return fail(KPOOL_ERR_INVALID_ARG, "k_norm_eps must be >= 0");
+    if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256))
+        return fail(KPOOL_ERR_WORKSPACE, "workspace of at least 256 bytes, 256-byte aligned, needed");
+    ProjectArgs a{};
+    a.x = x; a.w = w_kg; a.gamma = k_norm_weight; a.beta = k_norm_bias; a.ape = ape;
+    a.eps = k_norm_eps; a.cu_seqlens = cu_seqlens; a.cu_pools = cu_pools; a.n_docs = n_docs;
+    a.T = T; a.P_total = P_total; a.hidden = hidden; a.kpool = kpool;
+    a.pk_out = pk_out; a.k_out = k_out; a.gate_out = gate_out;
+    a.status = static_cast<int *>(workspace) + 1;
+    return run_project_compress(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kpool_score_topk_noalloc_status(int *status_out)
 {
     clear_error();

@@ -86,6 +86,21 @@ int score_capacity(int H, int D, int fp8);   // candidate slots per query (0 = u
 // Limit of one scoring-pipeline wait for later launches (0 = the 2 s
 // default); returns the previous limit.
 uint64_t set_wait_limit_ns(uint64_t ns);
+uint64_t get_wait_limit_ns();
+
+// The key path fused with compression (kpool_project.cu).
+struct ProjectArgs {
+    const void *x, *w;             // bf16 [T, hidden], bf16 [2D, hidden]
+    const float *gamma, *beta, *ape;
+    float eps;
+    const int32_t *cu_seqlens, *cu_pools;
+    int n_docs;
+    int64_t T, P_total;
+    int hidden, kpool;
+    void *pk_out, *k_out, *gate_out;
+    int *status;
+};
+int run_project_compress(const ProjectArgs &a, cudaStream_t s);
 int run_score(const ScoreArgs &a, cudaStream_t s);
 // Host-buffer pass with copies overlapped (kpool_pipeline.cu).  All input
 // pointers are host memory; cu_seqlens_host NULL means one sequence (n_docs =

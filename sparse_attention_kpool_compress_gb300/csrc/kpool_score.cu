@@ -1605,6 +1605,8 @@ uint64_t set_wait_limit_ns(uint64_t ns)
     return g_wait_limit_ns.exchange(ns == 0 ? kTimeoutNs : ns);
 }
 
+uint64_t get_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 int score_capacity(int H, int D, int fp8)
 {
     const Layout L = make_layout(H, D, fp8);

@@ -89,6 +89,14 @@ WORKLOADS = {
                                     "4194304 keys, H=64 D=128 kpool=4 index_topk=2048"),
 }
 
+# Key-path fusion (hidden states -> projected keys, k_norm, gate -> pooled keys):
+# the hidden size is not given by the pages; 6144 is used for measurement.
+PROJECTION_WORKLOADS = {
+    "proj_128k": dict(T=131072, hidden=6144, D=128, kpool=4,
+                      desc="Key path fused with compression: T=131072 hidden states of 6144, "
+                           "D=128, kpool=4 (x ~ N(0,1), W ~ N(0,1/hidden) bf16)"),
+}
+
 
 def doc_lengths(wl: Workload, gen: torch.Generator) -> list:
     if wl.n_docs == 1:
@@ -180,6 +188,41 @@ def make_inputs(wl: Workload, seed: int | None = None, T: int | None = None) -> 
         return Inputs(wl, cu_seqlens, q, k, gate, ape, w)
     return Inputs(wl, cu_seqlens, q, k, gate, ape, w,
                   torch.tensor(lay[0], dtype=torch.int32), torch.tensor(lay[1], dtype=torch.int32))
+
+
+@dataclass
+class ProjectionInputs:
+    """Inputs of the key path in front of compression (hidden states and the
+    key / gate projection weights, k_norm's weight and bias)."""
+    cu_seqlens: torch.Tensor      # int32 [n_docs + 1]
+    x: torch.Tensor               # bf16 [T, hidden]
+    w_kg: torch.Tensor            # bf16 [2D, hidden]: key projection rows, then gate rows
+    gamma: torch.Tensor           # fp32 [D]
+    beta: torch.Tensor            # fp32 [D]
+    ape: torch.Tensor             # fp32 [kpool, D]
+    eps: float = 1e-6
+
+
+def make_projection_inputs(T: int, hidden: int, D: int, kpool: int, n_docs: int = 1,
+                           doc_len_range=None, seed: int = 0) -> ProjectionInputs:
+    """Draw order (seeded torch.Generator on the CPU): document lengths (as for
+    packed-THD workloads), x ~ N(0, 1) and w_kg ~ N(0, 1/hidden) drawn in float32
+    and rounded to bfloat16, gamma = 1 + N(0, 0.1^2), beta ~ N(0, 0.1^2),
+    ape ~ N(0, 0.1^2)."""
+    wl = Workload("proj", T=T, H=1, D=D, kpool=kpool, index_topk=kpool, n_docs=n_docs,
+                  doc_len_range=doc_len_range)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    lens = doc_lengths(wl, gen)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    x = _normal_bf16((T, hidden), gen)
+    w_kg = _normal_bf16((2 * D, hidden), gen, scale=1.0 / math.sqrt(hidden))
+    gamma = 1.0 + 0.1 * torch.randn(D, generator=gen, dtype=torch.float32)
+    beta = 0.1 * torch.randn(D, generator=gen, dtype=torch.float32)
+    ape = 0.1 * torch.randn(kpool, D, generator=gen, dtype=torch.float32)
+    return ProjectionInputs(torch.tensor(cu, dtype=torch.int32), x, w_kg, gamma, beta, ape)
 
 
 def sample_rows(T: int, n_sample: int = 1024, edge: int = 64, seed: int = 0,
