@@ -23,10 +23,6 @@ What each function follows (page titles and sections):
   ``index_topk // kpool`` selection, ties to the lower pool index.
 * ``expand_rows`` -- expansion of pools to tokens plus the causal tail
   (``always_select_tail``).
-* ``sparse_attn`` -- the sparse attention that consumes the selection:
-  xtuner PR "GLM-5.3-Flash F5: NoPE DSA + KPool indexer", Summary (NoPE
-  sparse MLA, FlashMLA-style forward) and Megatron-LM PR section 3 (NoPE:
-  no rotary slice); absorbed form, keys and values are the latent rows.
 * ``project_keys`` -- the key path in front of compression: Megatron-LM PR
   Changes section 4 (linear_wk and k_norm in BF16, unquantized) and section
   3 / SkyRL commit "k-pool indexer" (the BF16 compression gate); k_norm is
@@ -99,7 +95,6 @@ def _load():
                                           i32, P, i64, P, P, P, P, P]),
             "ora_expand_rows_at": (None, [P, P, P, P, i32, i32, i32, i32, P, i64, P]),
             "ora_num_threads": (i32, []),
-            "ora_sparse_attn": (None, [P, P, P, i32, i32, i32, ctypes.c_double, P, i64, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -349,21 +344,3 @@ def expand_rows_at(sel, cu_q, q_pos, cu_k, kp: int, Kp: int, tail: bool, rows):
                                int(bool(tail)), _ptr(rows), n, _ptr(out))
     return out
 
-
-def sparse_attn(q_bits, c_bits, tok, scale: float, rows):
-    """Sparse attention over the selected tokens (absorbed NoPE form: keys and
-    values are the latent rows c).  q_bits bf16 [T, H, Dc], c_bits bf16 [Tk,
-    Dc], tok int32 [len(rows), W] token indices (-1 = none) for the query rows
-    `rows`.  Returns (o float64 [len(rows), H, Dc], lse float64 [len(rows), H])."""
-    q_bits = _c(q_bits, np.uint16)
-    c_bits = _c(c_bits, np.uint16)
-    tok = _c(tok, np.int32)
-    rows = _c(rows, np.int64)
-    T, H, Dc = q_bits.shape
-    n, W = tok.shape
-    assert n == len(rows) and c_bits.shape[1] == Dc
-    o = np.empty((n, H, Dc), np.float64)
-    lse = np.empty((n, H), np.float64)
-    _load().ora_sparse_attn(_ptr(q_bits), _ptr(c_bits), _ptr(tok), W, H, Dc, float(scale),
-                            _ptr(rows), n, _ptr(o), _ptr(lse))
-    return o, lse

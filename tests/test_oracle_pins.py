@@ -754,59 +754,3 @@ def test_project_keys_closed_forms(ora):
         assert np.allclose(k_ex[t], want, rtol=1e-14, atol=1e-15)
     assert not np.any(bf16_val(g))     # the gate column of x is zero
 
-
-# ---------------------------------------------------------------------------
-# The sparse attention that consumes the selection (absorbed NoPE form)
-# ---------------------------------------------------------------------------
-
-def _bits(t):
-    return W.bits(t)
-
-
-def _attn_inputs(T=40, H=3, Dc=16, seed=21):
-    gen = torch.Generator().manual_seed(seed)
-    q = torch.randn(T, H, Dc, generator=gen).to(torch.bfloat16)
-    c = torch.randn(T, Dc, generator=gen).to(torch.bfloat16)
-    return q, c
-
-
-def test_sparse_attn_matches_scipy_softmax(ora):
-    """Against scipy's softmax and logsumexp of numpy's float64 scores, on
-    random token subsets with -1 padding."""
-    from scipy.special import logsumexp, softmax
-    q, c = _attn_inputs()
-    qd, cd = q.double().numpy(), c.double().numpy()
-    rng = np.random.default_rng(3)
-    rows = np.array([5, 17, 39])
-    W = 12
-    tok = np.full((3, W), -1, np.int32)
-    for i, t in enumerate(rows):
-        sel = np.sort(rng.choice(t + 1, size=min(t + 1, 9), replace=False))
-        tok[i, :len(sel)] = sel
-    scale = 0.3
-    o, lse = ora.sparse_attn(_bits(q), _bits(c), tok, scale, rows)
-    for i, t in enumerate(rows):
-        sel = tok[i][tok[i] >= 0]
-        s = scale * qd[t] @ cd[sel].T                      # [H, n]
-        assert np.allclose(lse[i], logsumexp(s, axis=1), rtol=1e-13, atol=1e-13)
-        assert np.allclose(o[i], softmax(s, axis=1) @ cd[sel], rtol=1e-12, atol=1e-13)
-
-
-def test_sparse_attn_closed_forms(ora):
-    """One token: o is that token's latent row and lse its score; tokens with
-    identical latent rows: o is the row and lse = s + log(n); an order change
-    of the token list changes nothing; an empty row gives o = 0, lse = -inf."""
-    q, c = _attn_inputs(T=16, H=2, Dc=8)
-    qd, cd = q.double().numpy(), c.double().numpy()
-    tok = np.array([[7, -1, -1, -1], [-1, -1, -1, -1], [3, 9, 1, -1], [9, 1, -1, 3]], np.int32)
-    rows = np.array([10, 11, 12, 12])
-    o, lse = ora.sparse_attn(_bits(q), _bits(c), tok, 0.5, rows)
-    assert np.array_equal(o[0], np.tile(cd[7], (2, 1)))
-    assert np.allclose(lse[0], 0.5 * qd[10] @ cd[7], rtol=1e-15, atol=1e-15)
-    assert np.all(o[1] == 0) and np.all(np.isneginf(lse[1]))
-    assert np.allclose(o[2], o[3], rtol=1e-14, atol=1e-15) and np.allclose(lse[2], lse[3])
-    c_same = c.clone()
-    c_same[[1, 3, 9]] = c[4]
-    o2, lse2 = ora.sparse_attn(_bits(q), _bits(c_same), tok[2:3], 0.5, rows[2:3])
-    assert np.allclose(o2[0], np.tile(cd[4], (2, 1)), rtol=1e-14, atol=1e-15)
-    assert np.allclose(lse2[0], 0.5 * qd[12] @ cd[4] + math.log(3), rtol=1e-14)
