@@ -485,7 +485,7 @@ def main():
         q8 = torch.empty(T, H, D, dtype=torch.uint8, device=dev)
         qs = torch.empty(T, H, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    B = K.binding
+    from sparse_attention_kpool_compress_gb300 import binding as B
     L = B._lib
     sp = B._stream(dev)
 
@@ -718,7 +718,7 @@ def run_positioned(args, wl, inp, K, dev, world, rank, local):
     tok = torch.empty(Tq, Wd, dtype=torch.int32, device=dev)
     ws = K.new_workspace(Tq, H, n_docs, dev, kp, topk)
     stream = torch.cuda.current_stream(dev)
-    B = K.binding
+    from sparse_attention_kpool_compress_gb300 import binding as B
     L = B._lib
     sp = B._stream(dev)
 
@@ -979,7 +979,7 @@ def run_projection(args):
     P = T // kp
     pk = torch.empty(P, D, dtype=torch.bfloat16, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    B = K.binding
+    from sparse_attention_kpool_compress_gb300 import binding as B
     L = B._lib
     sp = B._stream(dev)
     stream = torch.cuda.current_stream(dev)
