@@ -472,6 +472,74 @@ __device__ void group_rank_store(float *cs, int *ci, int n, int pool_base, int w
     }
 }
 
+// Direct mode: the n scores of one query at their local pool positions
+// dq[0..n).  Writes the best k (ties to the lower pool index), or all n when
+// n <= k, to out_idx/out_score in ascending pool order and returns how many
+// it wrote.  One selection group: a radix search for the k-th key, then two
+// ordered passes (counts per warp, then ballot-ranked writes).
+__device__ int group_select_direct(const float *dq, int n, int k, int pool_base, int g, int gtid,
+                                   int *hist, int *gs, int32_t *out_idx, float *out_score)
+{
+    const int lane = gtid & 31, gw = gtid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    if (n <= k) {
+        for (int e = gtid; e < n; e += kGroupThreads) {
+            out_idx[e] = pool_base + e;
+            out_score[e] = dq[e];
+        }
+        return n;
+    }
+    uint32_t kth;
+    int above, inbin;
+    bool edge;
+    radix_kth(n, k, [&](int e) { return fkey(dq[e]); }, [](int) { return true; }, false, 0, g,
+              gtid, hist, gs, kth, above, inbin, edge);
+    // edge: the bin holds exactly the entries still needed -> keep key >= kth;
+    // otherwise keep key > kth and the first `need` entries equal to it
+    const int need = edge ? 0 : k - above;
+    group_bar(g);   // gs reuse
+    const int per_w = ((n + kGroupThreads - 1) / kGroupThreads) * 32;
+    const int r0 = gw * per_w, r1 = min(n, r0 + per_w);
+    int cgt = 0, ceq = 0;
+    for (int c = r0; c < r1; c += 32) {
+        const int e = c + lane;
+        const uint32_t key = e < r1 ? fkey(dq[e]) : 0u;
+        cgt += __popc(__ballot_sync(kFull, e < r1 && (edge ? key >= kth : key > kth)));
+        ceq += __popc(__ballot_sync(kFull, e < r1 && !edge && key == kth));
+    }
+    if (lane == 0) {
+        gs[16 + gw] = cgt;
+        gs[20 + gw] = ceq;
+    }
+    group_bar(g);
+    int base_gt = 0, base_eq = 0;
+    for (int w = 0; w < gw; ++w) {
+        base_gt += gs[16 + w];
+        base_eq += gs[20 + w];
+    }
+    int pos = base_gt + min(base_eq, need);
+    int eq_seen = base_eq;
+    for (int c = r0; c < r1; c += 32) {
+        const int e = c + lane;
+        const float v = e < r1 ? dq[e] : 0.f;
+        const uint32_t key = fkey(v);
+        const bool gt = e < r1 && (edge ? key >= kth : key > kth);
+        const bool eq = e < r1 && !edge && key == kth;
+        const unsigned beq = __ballot_sync(kFull, eq);
+        const bool keep = gt || (eq && eq_seen + __popc(beq & lt) < need);
+        const unsigned bk = __ballot_sync(kFull, keep);
+        if (keep) {
+            const int d = pos + __popc(bk & lt);
+            out_idx[d] = pool_base + e;
+            out_score[d] = v;
+        }
+        pos += __popc(bk);
+        eq_seen += __popc(beq);
+    }
+    group_bar(g);   // gs reuse by the caller
+    return k;
+}
+
 // Ascending sort of cs/ci[0..n) by pool index (ci), bitonic over the next
 // power of two (pad entries carry INT_MAX), by one group.  n2 <= capacity.
 __device__ void group_sort_by_pool(float *cs, int *ci, int n, int g, int gtid)
@@ -617,7 +685,7 @@ __device__ __noinline__ bool split_unit_end(const TileInfo *tu, int nq, int QT, 
 // kFew: the instantiation for calls with few query tiles (split-pool schedule,
 // lone-query tiles); the other one carries none of that code, which keeps the
 // main loop of long prefills as fast as it can be compiled.
-template <int H, bool kFew>
+template <int H, bool kFew, bool kDirect>
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_pk,
                  const __grid_constant__ Params p)
@@ -898,6 +966,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t *thr_s = reinterpret_cast<uint32_t *>(smem + L.thr_off);
         float *cs = reinterpret_cast<float *>(smem + L.cs_off);
         int *ci = reinterpret_cast<int *>(smem + L.ci_off);
+        float *cd = cs;                  // direct mode: query q's scores at cd[q * CD + pool]
+        const int CD = L.C;
         float *wsm = reinterpret_cast<float *>(smem + L.ws_off);  // 256 head weights
         float *part = wsm + kBN;                                   // [2][4][128] partial scores
         const ulonglong2 *w4 = reinterpret_cast<const ulonglong2 *>(wsm + sl * SLICE);
@@ -966,11 +1036,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nc[j] = min((tau0 + qbase + j + 1) / p.kp, t.pool_count);
             }
             bool aborted = false;
+            // Direct mode: when every visible pool of the tile's queries fits a
+            // query's candidate capacity C, scores are stored at their pool
+            // position and the final selection reads them in pool order (no
+            // appends, no compaction, no bitmap ranking).  Longer rows keep the
+            // threshold filter, whose compactions leave the final selection
+            // fewer entries than a row's full pool count.  Not for split units
+            // or a lone decode query.
+            const int nc_tile = min((tau0 + nq) / p.kp, t.pool_count);
+            const bool direct = kDirect && p.mode == 0 && nc_tile <= C;
 
             // The pool-tile loop.  (Counted from 0: a loop over [i0, i1), or one
             // with a per-warp branch, compiles to a slower body.)
             const int npt = t.i1 - t.i0;
-            auto tiles = [&]() {
+            auto tiles = [&](auto direct_tag) {
+            constexpr bool kDirect = decltype(direct_tag)::value;
             for (int i = 0; i < npt; ++i) {
                 PT_MARK(1);
                 aborted |= !wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy);
@@ -1053,6 +1133,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
 
+                if constexpr (kDirect) {
+                    // every visible pool's score at its pool position
+                    if (owner) {
+#pragma unroll
+                        for (int j = 0; j < QS; ++j) {
+                            const int qi = qbase + j;
+                            if (qi < nq && pool_local < nc[j]) cd[qi * CD + pool_local] = s[j];
+                        }
+                    }
+                    continue;
+                }
                 // survivors of the threshold filter, appended (unordered) with one
                 // shared-memory atomic per warp and query that has any
                 if (owner) {
@@ -1187,10 +1278,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
-                    tiles();
+                    tiles(std::false_type{});
                 }
+            } else if constexpr (kDirect) {
+                if (direct) tiles(std::true_type{});
+                else tiles(std::false_type{});
             } else {
-                tiles();
+                tiles(std::false_type{});
             }
             // after an abort the loop ran on to the tile's end without waiting
             // (its scores are garbage); all warps leave here together
@@ -1208,7 +1302,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           g, gtid, etid, misc + 2, p.part_idx, p.part_score,
                                           p.part_cnt, p.tile_ctr);
             }
-            for (int q = g; q < nq && emit; q += kGroups) {
+            for (int q = g; kDirect && q < nq && emit && direct; q += kGroups) {
+                const int64_t row = static_cast<int64_t>(t.t0 + q) * Kp;
+                const int nc_q = min((tau0 + q + 1) / p.kp, t.pool_count);
+                const int n = group_select_direct(cd + q * CD, nc_q, Kp, t.pool_base, g, gtid,
+                                                  hist, gs, p.pool_idx + row, p.pool_score + row);
+                for (int e = n + gtid; e < Kp; e += kGroupThreads) {
+                    p.pool_idx[row + e] = -1;
+                    p.pool_score[row + e] = -INFINITY;
+                }
+            }
+            for (int q = g; q < nq && emit && !direct; q += kGroups) {
                 int n = qcnt[q];
                 float *csq = cs + q * C;
                 int *ciq = ci + q * C;
@@ -1483,25 +1587,30 @@ int encode_2d(CUtensorMap *m, const void *base, int fp8, uint64_t cols, uint64_t
     return KPOOL_OK;
 }
 
-template <int H, bool kFew>
+template <int H, bool kFew, bool kDirect>
 int launch_hf(const Layout &L, const CUtensorMap &mq, const CUtensorMap &mpk, const Params &prm,
               int grid, cudaStream_t s)
 {
     const int smem = static_cast<int>(L.total) + 1024;
-    KPOOL_CUDA_CHECK(cudaFuncSetAttribute(score_kernel<H, kFew>,
+    KPOOL_CUDA_CHECK(cudaFuncSetAttribute(score_kernel<H, kFew, kDirect>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    score_kernel<H, kFew><<<grid, kThreads, smem, s>>>(mq, mpk, prm);
+    score_kernel<H, kFew, kDirect><<<grid, kThreads, smem, s>>>(mq, mpk, prm);
     KPOOL_CUDA_CHECK(cudaGetLastError());
     return KPOOL_OK;
 }
 
+// Three instantiations: the split-pool schedule for calls with few query
+// tiles; direct mode for calls whose documents are short on average (at most
+// 4C pools each: their short tiles skip the threshold filter); and the long
+// prefill loop, which carries no code of the other two.
 template <int H>
 int launch_h(const ScoreArgs &a, const Layout &L, const CUtensorMap &mq, const CUtensorMap &mpk,
              const Params &prm, int grid, cudaStream_t s)
 {
-    (void)a;
-    return prm.units != nullptr ? launch_hf<H, true>(L, mq, mpk, prm, grid, s)
-                                : launch_hf<H, false>(L, mq, mpk, prm, grid, s);
+    if (prm.units != nullptr) return launch_hf<H, true, false>(L, mq, mpk, prm, grid, s);
+    if (a.mode == 0 && a.P_total <= 4 * static_cast<int64_t>(L.C) * a.n_docs)
+        return launch_hf<H, false, true>(L, mq, mpk, prm, grid, s);
+    return launch_hf<H, false, false>(L, mq, mpk, prm, grid, s);
 }
 
 // Scratch of the allocation-free entry point (kpool_score_topk_noalloc): the
