@@ -971,6 +971,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *wsm = reinterpret_cast<float *>(smem + L.ws_off);  // 256 head weights
         float *part = wsm + kBN;                                   // [2][4][128] partial scores
         const ulonglong2 *w4 = reinterpret_cast<const ulonglong2 *>(wsm + sl * SLICE);
+        // H >= 32: the accumulator is read with the 16x256b shape, so a thread holds 4
+        // pools x 16 head columns (columns 8j + 2kq, +1) and keeps its 16 head weights
+        // in registers for the whole query tile; the 4 threads of a quad (same rq)
+        // finish each pool's head sum with a 2-step transpose-reduce, after which
+        // thread (rq, kq) owns pool lane rq + 8 * (2 * (kq & 1) + (kq >> 1)).
+        constexpr bool kQL = H >= 32;
+        const int kq = lane & 3, rq = lane >> 2;
+        const int own = kQL ? rq + 8 * (2 * (kq & 1) + (kq >> 1)) : lane;
+        uint64_t wq[kQL ? 8 : 1];
         const int C = L.C;
         const int Kp = p.Kp;
         const int slack = max(0, min(kSlack, C - kBM - Kp));
@@ -1027,6 +1036,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::named_bar_sync(1, kEpiThreads);
             if (*agree_ti != 0u || t.t0 < 0) break;   // the same outcome in every warp
+            if constexpr (kQL) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float2 wv2 = *reinterpret_cast<const float2 *>(wsm + sl * SLICE + 8 * j + 2 * kq);
+                    wq[j] = ptx::pack_f32x2(wv2.x, wv2.y);
+                }
+            }
 
             uint32_t thr[QS];
             int nc[QS];
@@ -1046,6 +1062,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nc_tile = min((tau0 + nq) / p.kp, t.pool_count);
             const bool direct = kDirect && p.mode == 0 && nc_tile <= C;
 
+            // Head sums of accumulator `acc_sel` for this thread's pool(s) (H >= 32):
+            // relu(x) * w over the warp's 64 columns, then the quad transpose-reduce.
+            // Releases the accumulator once its TMEM reads are done.
+            auto head_sums_ql = [&](uint32_t acc_sel, float (&s_out)[QS]) {
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) +
+                                    acc_sel * kAccCols + sl * SLICE;
+                uint32_t va[32], vb[32];
+                ptx::tmem_ld16x256_x8(tb, va);
+                ptx::tmem_ld16x256_x8(tb + (16u << 16), vb);
+                ptx::tmem_ld_wait2(va, vb);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc_sel));
+                uint64_t a[QS][4];
+#pragma unroll
+                for (int j = 0; j < QS; ++j)
+#pragma unroll
+                    for (int l = 0; l < 4; ++l) a[j][l] = 0ull;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int qj = kHalfQ ? 0 : (8 * j) / H;
+                    a[qj][0] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(va[4 * j]), 0.f),
+                                                          fmaxf(__uint_as_float(va[4 * j + 1]), 0.f)),
+                                          wq[j], a[qj][0]);
+                    a[qj][1] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(va[4 * j + 2]), 0.f),
+                                                          fmaxf(__uint_as_float(va[4 * j + 3]), 0.f)),
+                                          wq[j], a[qj][1]);
+                    a[qj][2] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(vb[4 * j]), 0.f),
+                                                          fmaxf(__uint_as_float(vb[4 * j + 1]), 0.f)),
+                                          wq[j], a[qj][2]);
+                    a[qj][3] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(vb[4 * j + 2]), 0.f),
+                                                          fmaxf(__uint_as_float(vb[4 * j + 3]), 0.f)),
+                                          wq[j], a[qj][3]);
+                }
+                const bool b0 = (kq & 1) != 0, b1 = (kq & 2) != 0;
+#pragma unroll
+                for (int j = 0; j < QS; ++j) {
+                    const float s0 = ptx::sum_f32x2(a[j][0]), s1 = ptx::sum_f32x2(a[j][1]);
+                    const float s2 = ptx::sum_f32x2(a[j][2]), s3 = ptx::sum_f32x2(a[j][3]);
+                    // step 1 (partner kq ^ 1): keep lanes {0, 8} or {16, 24}
+                    const float r0 = __shfl_xor_sync(kFull, b0 ? s0 : s2, 1);
+                    const float r1 = __shfl_xor_sync(kFull, b0 ? s1 : s3, 1);
+                    const float t0 = (b0 ? s2 : s0) + r0;
+                    const float t1 = (b0 ? s3 : s1) + r1;
+                    // step 2 (partner kq ^ 2): keep one of the two
+                    const float r2 = __shfl_xor_sync(kFull, b1 ? t0 : t1, 2);
+                    s_out[j] = (b1 ? t1 : t0) + r2;
+                }
+            };
+
             // The pool-tile loop.  (Counted from 0: a loop over [i0, i1), or one
             // with a per-warp branch, compiles to a slower body.)
             const int npt = t.i1 - t.i0;
@@ -1056,6 +1122,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 aborted |= !wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy);
                 PT_MARK(2);
                 ptx::tc_fence_after();
+                float s[QS];
+                if constexpr (kQL) {
+                    head_sums_ql(acc, s);
+                    if (++acc == 2) { acc = 0; acc_ph ^= 1; }
+                } else {
                 // relu(x) * w summed per query over this warp's 64 columns
                 uint64_t a4[QS][NACC];
 #pragma unroll
@@ -1091,10 +1162,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     accum(v1, 32);
                 }
                 if (++acc == 2) { acc = 0; acc_ph ^= 1; }
-
-                const int pool_local = (i + t.i0) * kBM + qr * 32 + lane;
-                const int pool_g = t.pool_base + pool_local;
-                float s[QS];
 #pragma unroll
                 for (int j = 0; j < QS; ++j) {
                     float v = ptx::sum_f32x2(a4[j][0]);
@@ -1102,12 +1169,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 1; k < NACC; ++k) v += ptx::sum_f32x2(a4[j][k]);
                     s[j] = v;
                 }
+                }
+
+                const int pool_local = (i + t.i0) * kBM + qr * 32 + own;
+                const int pool_g = t.pool_base + pool_local;
                 if (kHalfQ) {
                     // the two 64-head halves of a query meet in shared memory
                     float *pt = part + (tile_seq & 1) * (4 * kBM);
-                    pt[sl * kBM + qr * 32 + lane] = s[0];
+                    pt[sl * kBM + qr * 32 + own] = s[0];
                     ptx::named_bar_sync(1, kEpiThreads);
-                    if (owner) s[0] += pt[(sl + 1) * kBM + qr * 32 + lane];
+                    if (owner) s[0] += pt[(sl + 1) * kBM + qr * 32 + own];
                 }
                 ++tile_seq;
                 float sk = 1.f;
@@ -1203,47 +1274,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         aborted |= !wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy);
                         PT_MARK(2);
                         ptx::tc_fence_after();
-                        uint64_t a4[NACC];
-#pragma unroll
-                        for (int k = 0; k < NACC; ++k) a4[k] = 0ull;
-                        {
-                            const uint32_t tb = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) +
-                                                acc * kAccCols + sl * SLICE;
-                            uint32_t v0[32], v1[32];
-                            ptx::tmem_ld32(tb, v0);
-                            ptx::tmem_ld32(tb + 32, v1);
-                            ptx::tmem_ld_wait2(v0, v1);
-                            ptx::tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) ptx::mbar_arrive(bar(BTM_EMPTY + acc));
-#pragma unroll
-                            for (int x = 0; x < 64; x += 4) {
-                                const uint32_t *v = x < 32 ? v0 : v1;
-                                const int xx = x & 31;
-                                const ulonglong2 wv = w4[x / 4];
-                                const uint64_t r0 = ptx::pack_f32x2(
-                                    fmaxf(__uint_as_float(v[xx]), 0.f),
-                                    fmaxf(__uint_as_float(v[xx + 1]), 0.f));
-                                const uint64_t r1 = ptx::pack_f32x2(
-                                    fmaxf(__uint_as_float(v[xx + 2]), 0.f),
-                                    fmaxf(__uint_as_float(v[xx + 3]), 0.f));
-                                a4[(x / 4) % NACC] = ptx::ffma2(r0, wv.x, a4[(x / 4) % NACC]);
-                                a4[(x / 4) % NACC] = ptx::ffma2(r1, wv.y, a4[(x / 4) % NACC]);
-                            }
-                        }
+                        float svq[QS];
+                        head_sums_ql(acc, svq);   // kQuad implies H >= 64
                         if (++acc == 2) { acc = 0; acc_ph ^= 1; }
-                        float sv = ptx::sum_f32x2(a4[0]);
-#pragma unroll
-                        for (int k = 1; k < NACC; ++k) sv += ptx::sum_f32x2(a4[k]);
+                        float sv = svq[0];
                         if (kHalfQ) {
                             float *pt = part + (tile_seq & 1) * (4 * kBM);
-                            pt[sl * kBM + qr * 32 + lane] = sv;
+                            pt[sl * kBM + qr * 32 + own] = sv;
                             ptx::named_bar_sync(1, kEpiThreads);
-                            if (owner) sv += pt[(sl + 1) * kBM + qr * 32 + lane];
+                            if (owner) sv += pt[(sl + 1) * kBM + qr * 32 + own];
                         }
                         ++tile_seq;
                         const int tj = m * QT + qbase;   // this warp's pool tile of the unit
-                        const int pool_local = (t.i0 + tj) * kBM + qr * 32 + lane;
+                        const int pool_local = (t.i0 + tj) * kBM + qr * 32 + own;
                         const int pool_g = t.pool_base + pool_local;
                         if (p.fp8 && pool_g < p.P_total) sv *= p.pk_scale[pool_g];
                         sv = (sv == 0.f) ? 0.f : sv;   // fold -0 into +0
