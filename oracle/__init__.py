@@ -23,6 +23,12 @@ What each function follows (page titles and sections):
   ``index_topk // kpool`` selection, ties to the lower pool index.
 * ``expand_rows`` -- expansion of pools to tokens plus the causal tail
   (``always_select_tail``).
+* ``sparse_attn`` -- the sparse attention that consumes the selection:
+  xtuner PR "GLM-5.3-Flash F5: NoPE DSA + KPool indexer + clamped
+  SwiGLU", Summary (NoPE sparse attention, a FlashMLA-style SparseMLA
+  forward over the selected tokens) and Megatron-LM PR Changes section 3
+  ("NoPE": no positional slice in the absorbed query); in the absorbed
+  form the latent rows are both keys and values.
 * ``project_keys`` -- the key path in front of compression: Megatron-LM PR
   Changes section 4 (linear_wk and k_norm in BF16, unquantized) and section
   3 / SkyRL commit "k-pool indexer" (the BF16 compression gate); k_norm is
@@ -95,6 +101,7 @@ def _load():
                                           i32, P, i64, P, P, P, P, P]),
             "ora_expand_rows_at": (None, [P, P, P, P, i32, i32, i32, i32, P, i64, P]),
             "ora_num_threads": (i32, []),
+            "ora_sparse_attn": (None, [P, P, P, i32, i32, i32, ctypes.c_double, P, i64, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -344,3 +351,22 @@ def expand_rows_at(sel, cu_q, q_pos, cu_k, kp: int, Kp: int, tail: bool, rows):
                                int(bool(tail)), _ptr(rows), n, _ptr(out))
     return out
 
+
+def sparse_attn(q_bits, c_bits, tok, scale: float, rows):
+    """Sparse attention over the selected tokens (absorbed NoPE form: keys and
+    values are the latent rows c).  q_bits bf16 bits [T, H, Dc], c_bits bf16
+    bits [Tk, Dc], tok int32 [len(rows), W] token indices (-1 = none) for the
+    query rows `rows`.  Returns (o float64 [len(rows), H, Dc], lse float64
+    [len(rows), H]); lse is the natural-log sum of exp of the scaled scores."""
+    q_bits = _c(q_bits, np.uint16)
+    c_bits = _c(c_bits, np.uint16)
+    tok = _c(tok, np.int32)
+    rows = _c(rows, np.int64)
+    T, H, Dc = q_bits.shape
+    n, W = tok.shape
+    assert n == len(rows) and c_bits.shape[1] == Dc
+    o = np.empty((n, H, Dc), np.float64)
+    lse = np.empty((n, H), np.float64)
+    _load().ora_sparse_attn(_ptr(q_bits), _ptr(c_bits), _ptr(tok), W, H, Dc, float(scale),
+                            _ptr(rows), n, _ptr(o), _ptr(lse))
+    return o, lse

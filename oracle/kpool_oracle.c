@@ -688,6 +688,62 @@ void ora_expand_rows(const int32_t *sel, const int32_t *cu_seqlens, int n_docs, 
     ora_expand_rows_at(sel, cu_seqlens, NULL, cu_seqlens, n_docs, kp, Kp, tail, rows, n_rows, out);
 }
 
+/* ------------------------------------------------------------------ */
+/* The sparse attention that consumes the indexer's selection: xtuner   */
+/* PR "GLM-5.3-Flash F5: NoPE DSA + KPool indexer + clamped SwiGLU",    */
+/* Summary (NoPE DeepSeek sparse attention; a SparseMLA forward of the  */
+/* FlashMLA kind over the selected token indices) and Megatron-LM PR    */
+/* "GLM5.3 Flash", Changes section 3, "NoPE" (the absorbed query has no */
+/* positional slice).  In the absorbed form every head of query t       */
+/* attends over the latent rows c[j] of the selected tokens, which      */
+/* serve as keys and as values:                                         */
+/*   s_j   = scale * sum_d q[t, h, d] * c[j, d]      j in tok[r, :], j >= 0 */
+/*   lse   = log sum_j exp(s_j)                                         */
+/*   o[d]  = sum_j exp(s_j - lse) * c[j, d]                             */
+/* in double.  A listed index counts once per listing; -1 entries are   */
+/* skipped; a row without tokens gets o = 0 and lse = -inf.             */
+/* ------------------------------------------------------------------ */
+void ora_sparse_attn(const uint16_t *q, const uint16_t *c, const int32_t *tok, int W, int H,
+                     int Dc, double scale, const int64_t *rows, int64_t n_rows, double *o_out,
+                     double *lse_out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; r++) {
+        const int64_t t = rows[r];
+        const int32_t *tr = tok + r * (int64_t)W;
+        double *s = (double *)malloc(sizeof(double) * (W > 0 ? W : 1));
+        for (int h = 0; h < H; h++) {
+            const uint16_t *qh = q + (t * H + h) * (int64_t)Dc;
+            double m = -INFINITY;
+            for (int j = 0; j < W; j++) {
+                if (tr[j] < 0) continue;
+                double acc = 0.0;
+                for (int d = 0; d < Dc; d++)
+                    acc += ora_bf16_to_double(qh[d]) * ora_bf16_to_double(c[(int64_t)tr[j] * Dc + d]);
+                s[j] = scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double *oh = o_out + (r * H + h) * (int64_t)Dc;
+            for (int d = 0; d < Dc; d++) oh[d] = 0.0;
+            if (m == -INFINITY) {
+                lse_out[r * H + h] = -INFINITY;
+                continue;
+            }
+            double z = 0.0;
+            for (int j = 0; j < W; j++)
+                if (tr[j] >= 0) z += exp(s[j] - m);
+            for (int j = 0; j < W; j++) {
+                if (tr[j] < 0) continue;
+                const double p = exp(s[j] - m) / z;
+                for (int d = 0; d < Dc; d++)
+                    oh[d] += p * ora_bf16_to_double(c[(int64_t)tr[j] * Dc + d]);
+            }
+            lse_out[r * H + h] = m + log(z);
+        }
+        free(s);
+    }
+}
+
 int ora_num_threads(void)
 {
 #ifdef _OPENMP

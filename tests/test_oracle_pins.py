@@ -754,3 +754,117 @@ def test_project_keys_closed_forms(ora):
         assert np.allclose(k_ex[t], want, rtol=1e-14, atol=1e-15)
     assert not np.any(bf16_val(g))     # the gate column of x is zero
 
+
+
+# ---------------------------------------------------------------------------
+# The sparse attention that consumes the selection (absorbed NoPE form)
+# ---------------------------------------------------------------------------
+
+def _frac(x: str) -> float:
+    if "/" in x:
+        a, b = x.split("/")
+        return float(a) / float(b)
+    return float(x)
+
+
+def _ln(x: str) -> float:
+    x = x.strip()
+    if x == "-inf":
+        return -math.inf
+    assert x.startswith("ln ")
+    return math.log(_frac(x[3:]))
+
+
+def sparse_attn_worked():
+    """tests/golden/sparse_attn_worked.txt: the token table {j: (c0, c1)} and
+    the cases (scale, q0, indices, o0, o1, lse)."""
+    table, cases = {}, []
+    for line in open(os.path.join(GOLDEN, "sparse_attn_worked.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        f = [x.strip() for x in line.split("|")]
+        if f[0] == "token":
+            table[int(f[1])] = (_frac(f[2]), _frac(f[3]))
+        else:
+            assert f[0] == "case"
+            cases.append((_ln(f[1]), _frac(f[2]), [int(v) for v in f[3].split()],
+                          _frac(f[4]), _frac(f[5]), _ln(f[6])))
+    return table, cases
+
+
+def sparse_attn_worked_inputs(q0, idx, table, H=2, Dc=8, Tq=1):
+    """BF16 q [Tq, H, Dc] with q[:, :, 0] = q0, latent rows [len(table), Dc]
+    with dims 0 and 1 from the table, and the index row padded to itself."""
+    c = torch.zeros(len(table), Dc)
+    for j, (a, v) in table.items():
+        c[j, 0], c[j, 1] = a, v
+    q = torch.zeros(Tq, H, Dc)
+    q[:, :, 0] = q0
+    return q.to(torch.bfloat16), c.to(torch.bfloat16), np.array([idx], np.int32)
+
+
+def test_sparse_attn_hand_worked(ora):
+    """Hand-worked weights at moderate scores (tests/golden/sparse_attn_worked.txt)."""
+    table, cases = sparse_attn_worked()
+    assert len(cases) == 6
+    for scale, q0, idx, o0, o1, lse in cases:
+        q, c, tok = sparse_attn_worked_inputs(q0, idx, table)
+        o, l = ora.sparse_attn(W.bits(q), W.bits(c), tok, scale, np.array([0]))
+        want = np.zeros((2, 8))
+        want[:, 0], want[:, 1] = o0, o1
+        assert np.allclose(o[0], want, rtol=1e-13, atol=1e-14), (idx, o[0, 0, :2])
+        if math.isinf(lse):
+            assert np.all(np.isneginf(l[0]))
+        else:
+            assert np.allclose(l[0], lse, rtol=1e-13, atol=1e-14)
+
+
+def _attn_inputs(T=40, H=3, Dc=16, seed=21):
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(T, H, Dc, generator=gen).to(torch.bfloat16)
+    c = torch.randn(T, Dc, generator=gen).to(torch.bfloat16)
+    return q, c
+
+
+def test_sparse_attn_matches_scipy_softmax(ora):
+    """Against scipy's softmax and logsumexp of numpy's float64 scores, on
+    random token subsets with -1 padding (the softmax runs over the tokens of
+    each head separately)."""
+    from scipy.special import logsumexp, softmax
+    q, c = _attn_inputs()
+    qd, cd = q.double().numpy(), c.double().numpy()
+    rng = np.random.default_rng(3)
+    rows = np.array([5, 17, 39])
+    Wd = 12
+    tok = np.full((3, Wd), -1, np.int32)
+    for i, t in enumerate(rows):
+        sel = np.sort(rng.choice(t + 1, size=min(t + 1, 9), replace=False))
+        tok[i, :len(sel)] = sel
+    scale = 0.3
+    o, lse = ora.sparse_attn(W.bits(q), W.bits(c), tok, scale, rows)
+    for i, t in enumerate(rows):
+        sel = tok[i][tok[i] >= 0]
+        s = scale * qd[t] @ cd[sel].T                      # [H, n]
+        assert np.allclose(lse[i], logsumexp(s, axis=1), rtol=1e-13, atol=1e-13)
+        assert np.allclose(o[i], softmax(s, axis=1) @ cd[sel], rtol=1e-12, atol=1e-13)
+
+
+def test_sparse_attn_closed_forms(ora):
+    """One token: o is that token's latent row and lse its score; tokens with
+    identical latent rows: o is the row and lse = s + log(n); an order change
+    of the token list changes nothing; an empty row gives o = 0, lse = -inf."""
+    q, c = _attn_inputs(T=16, H=2, Dc=8)
+    qd, cd = q.double().numpy(), c.double().numpy()
+    tok = np.array([[7, -1, -1, -1], [-1, -1, -1, -1], [3, 9, 1, -1], [9, 1, -1, 3]], np.int32)
+    rows = np.array([10, 11, 12, 12])
+    o, lse = ora.sparse_attn(W.bits(q), W.bits(c), tok, 0.5, rows)
+    assert np.array_equal(o[0], np.tile(cd[7], (2, 1)))
+    assert np.allclose(lse[0], 0.5 * qd[10] @ cd[7], rtol=1e-15, atol=1e-15)
+    assert np.all(o[1] == 0) and np.all(np.isneginf(lse[1]))
+    assert np.allclose(o[2], o[3], rtol=1e-14, atol=1e-15) and np.allclose(lse[2], lse[3])
+    c_same = c.clone()
+    c_same[[1, 3, 9]] = c[4]
+    o2, lse2 = ora.sparse_attn(W.bits(q), W.bits(c_same), tok[2:3], 0.5, rows[2:3])
+    assert np.allclose(o2[0], np.tile(cd[4], (2, 1)), rtol=1e-14, atol=1e-15)
+    assert np.allclose(lse2[0], 0.5 * qd[12] @ cd[4] + math.log(3), rtol=1e-14)
