@@ -410,6 +410,143 @@ def timed_loop(step, n_seg, steps, stream, in_bytes, local, barrier):
     return ms_step, segs, clocks, note
 
 
+def run_mla(args):
+    """The sparse attention that consumes the selection, fused with the
+    expansion (kpool_sparse_mla_fwd_pools): one call per step over the whole
+    workload, on the indexer's own selection (computed once, untimed).
+    Tensor-bound: 4 * H * Dc FLOPs per (query, listed token) pair (scores and
+    output), counted over the valid listed tokens."""
+    wl = W.MLA_WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm covers the indexer "
+                          "workloads; the sparse attention reports its oracle sample as "
+                          "cpu_baseline"}), flush=True)
+        return 0
+    torch.cuda.set_device(local)
+    import sparse_attention_kpool_compress_gb300 as K
+    from sparse_attention_kpool_compress_gb300 import binding as B
+    dev = torch.device("cuda", local)
+    inp = W.make_inputs(wl, seed=wl.seed)
+    cu_d = cp_d = P = None
+    if wl.n_docs > 1:
+        cp_h, P = K.kpool_num_pools(inp.cu_seqlens, wl.T, wl.kpool)
+        cu_d, cp_d = inp.cu_seqlens.to(dev), cp_h.to(dev)
+    _, pool_idx, _ = K.kpool_indexer_forward(inp.q.to(dev), inp.k.to(dev), inp.gate.to(dev),
+                                             inp.ape.to(dev), inp.w.to(dev), wl.kpool,
+                                             wl.index_topk, wl.tail, cu_d, cp_d, P)
+    mi = W.make_mla_inputs(wl.T, seed=wl.seed)
+    q, kv = mi.q.to(dev), mi.kv.to(dev)
+    T, H, Dc = q.shape
+    o = torch.empty(T, H, Dc, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    ws = torch.zeros(K.kpool_sparse_mla_workspace_size(), dtype=torch.uint8, device=dev)
+    # listed tokens per row: the selected pools' tokens plus the tail
+    if cu_d is None:
+        tau = torch.arange(T, device=dev)
+    else:
+        starts = inp.cu_seqlens.to(dev).long()
+        doc = torch.searchsorted(starts[1:], torch.arange(T, device=dev), right=True)
+        tau = torch.arange(T, device=dev) - starts[doc]
+    n_tok = (pool_idx >= 0).sum(dim=1).long() * wl.kpool
+    if wl.tail:
+        n_tok += (tau + 1) % wl.kpool
+    pairs = int(n_tok.sum().item())
+    flops = 4.0 * H * Dc * pairs
+    L = B._lib
+    sp = B._stream(dev)
+    stream = torch.cuda.current_stream(dev)
+    n_docs = wl.n_docs if cu_d is not None else 1
+
+    def call():
+        rc = L.kpool_sparse_mla_fwd_pools(B._ptr(q), B._ptr(kv), B._ptr(pool_idx), B._ptr(cu_d),
+                                          B._ptr(cp_d), n_docs, T, H, Dc, wl.kpool,
+                                          wl.index_topk, int(wl.tail), ctypes.c_float(mi.scale),
+                                          B._ptr(o), B._ptr(lse), B._ptr(ws), ws.numel(), sp)
+        if rc != 0:
+            raise B.KPoolError(rc, "kpool_sparse_mla_fwd_pools")
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        call()
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if K.kpool_read_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    in_bytes = q.numel() * 2 + kv.numel() * 2 + pool_idx.numel() * 4
+    ms, _, clocks, l2_note = timed_loop(step, 1, args.steps, stream, in_bytes, local,
+                                        lambda: None)
+    peaks, peak_src = load_peaks()
+    tflops = flops / ms / 1e9
+    e2e = None
+    if not args.no_e2e:
+        hq, hkv = mi.q.pin_memory(), mi.kv.pin_memory()
+        hsel = pool_idx.cpu().pin_memory()
+        ho = torch.empty(T, H, Dc, dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty(T, H, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            kv.copy_(hkv, non_blocking=True)
+            pool_idx.copy_(hsel, non_blocking=True)
+            call()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(5):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        me = a0.elapsed_time(a1) / 5
+        e2e = {"value": T / (me / 1000.0), "unit": "queries/s", "ms_per_step": me, "steps": 5,
+               "h2d_bytes_per_step": (hq.numel() + hkv.numel()) * 2 + hsel.numel() * 4,
+               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4}
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle as ora
+        ora.build()
+        rows = W.sample_rows(T, n_sample=4, edge=0, seed=1).numpy()
+        rows = rows[rows >= T // 2][:4]
+        sel = pool_idx.cpu().numpy()[rows]
+        tok = ora.expand_rows(sel, inp.cu_seqlens.numpy() if cu_d is not None else None, T,
+                              wl.kpool, wl.Kp, wl.tail, rows)
+        t0 = time.time()
+        ora.sparse_attn(W.bits(mi.q), W.bits(mi.kv), tok, mi.scale, rows)
+        dt = time.time() - t0
+        cpu = {"value": len(rows) / dt, "unit": "queries/s", "cores": ora.num_threads(),
+               "kind": "oracle", "sample": "%d query rows of the second half (%d listed tokens "
+               "each at most), fp64 C" % (len(rows), wl.Kp * wl.kpool + wl.kpool - 1)}
+    line = {
+        "metric": "Sparse attention over the KPool selection (absorbed NoPE MLA, fused "
+                  "expansion), queries/s", "value": T / (ms / 1000.0),
+        "unit": "queries/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "desc": wl.desc, "T": T, "heads": H, "latent": Dc,
+                   "kpool": wl.kpool, "index_topk": wl.index_topk, "tail": wl.tail,
+                   "n_docs": wl.n_docs, "parallelism": "single", "l2": l2_note},
+        "e2e": e2e, "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "kernel": "sparse_mla_kernel", "achieved": tflops,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tflops / peaks["bf16_tflops"],
+                     "frac_of_sustained": tflops / peaks["bf16_tflops_sustained"],
+                     "traffic": None, "peak_source": "bf16 burst (%s)" % peak_src,
+                     "algorithmic_flops_per_launch": flops, "listed_tokens": pairs},
+        "cpu_baseline": cpu, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,7 +554,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_128k",
-                    choices=sorted(W.WORKLOADS) + sorted(W.PROJECTION_WORKLOADS))
+                    choices=sorted(W.WORKLOADS) + sorted(W.PROJECTION_WORKLOADS) +
+                    sorted(W.MLA_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--baseline-rows", type=int, default=3584)
@@ -438,6 +576,8 @@ def main():
         args.warmup = 3
     if args.workload in W.PROJECTION_WORKLOADS:
         return run_projection(args)
+    if args.workload in W.MLA_WORKLOADS:
+        return run_mla(args)
     wl = W.WORKLOADS[args.workload]
     if args.T is not None:
         from dataclasses import replace

@@ -390,6 +390,72 @@ KPOOL_API int kpool_indexer_forward_host(const void *q, const void *k, const voi
                                          size_t scratch_bytes, kpool_stream_t stream);
 
 /*
+ * Sparse attention over the selection: the absorbed NoPE MLA forward that
+ * consumes the indexer's output (xtuner PR "GLM-5.3-Flash F5: NoPE DSA +
+ * KPool indexer + clamped SwiGLU", Summary: a FlashMLA-style SparseMLA
+ * forward over the selected token indices, 64 heads in the production
+ * config, head and value width 512 once the rotary slice is gone; Megatron-LM
+ * PR section 3, "NoPE": the absorbed query has no positional slice).  Keys and
+ * values are the same latent rows kv[j].  For query row t and head h, over the
+ * row's token list J(t):
+ *     s_j        = softmax_scale * sum_d q[t, h, d] * kv[j, d]     (FP32)
+ *     o[t, h, :] = sum_j softmax_j(s) kv[j, :]                      (BF16 out)
+ *     lse[t, h]  = ln sum_j exp(s_j)                                (FP32 out)
+ * A listed index counts once per listing; -1 entries (and indices outside
+ * [0, Tk)) are skipped; a row with no token gets o = 0 and lse = -inf.
+ * Arithmetic: tcgen05 MMAs with FP32 accumulation; the softmax weights are
+ * rounded to BF16 before they multiply kv (the sums use the FP32 weights).
+ *   q            bf16 [T, H, Dc] absorbed queries, 16-byte aligned
+ *   kv           bf16 [Tk, Dc] latent rows, 16-byte aligned
+ *   o_out        bf16 [T, H, Dc], 16-byte aligned;  lse_out fp32 [T, H]
+ *   workspace    >= kpool_sparse_mla_workspace_size() bytes, 256-byte
+ *                aligned; its status word (kpool_read_status) reports a
+ *                pipeline timeout (KPOOL_STATUS_TIMEOUT: outputs invalid)
+ * Supported: H = 64, Dc = 512 (UNSUPPORTED otherwise); softmax_scale finite
+ * and > 0.
+ *
+ * kpool_sparse_mla_fwd -- J(t) is row t of tok_idx (int32 [T, W], as written
+ * by kpool_expand_indices, or any list with -1 padding).
+ */
+KPOOL_API size_t kpool_sparse_mla_workspace_size(void);
+KPOOL_API int kpool_sparse_mla_fwd(const void *q, const void *kv, const int32_t *tok_idx,
+                                   int64_t T, int64_t Tk, int W, int H, int Dc,
+                                   float softmax_scale, void *o_out, float *lse_out,
+                                   void *workspace, size_t workspace_bytes, kpool_stream_t stream);
+
+/*
+ * kpool_sparse_mla_fwd_pools -- the same attention fused with the expansion:
+ * J(t) is what kpool_expand_indices would write for row t of pool_idx (the
+ * selected pools' kpool tokens in order, then the causal tail when
+ * always_select_tail), built on the fly so that the token table never
+ * reaches memory.  Keys are the query tokens themselves (Tk = T).
+ * pool_idx int32 [T, index_topk / kpool] as written by kpool_score_topk
+ * (a row's first min(n_c, Kp) entries are its pools); cu_seqlens, cu_pools,
+ * n_docs as kpool_expand_indices.
+ */
+KPOOL_API int kpool_sparse_mla_fwd_pools(const void *q, const void *kv, const int32_t *pool_idx,
+                                         const int32_t *cu_seqlens, const int32_t *cu_pools,
+                                         int n_docs, int64_t T, int H, int Dc, int kpool,
+                                         int index_topk, int always_select_tail,
+                                         float softmax_scale, void *o_out, float *lse_out,
+                                         void *workspace, size_t workspace_bytes,
+                                         kpool_stream_t stream);
+
+/*
+ * kpool_sparse_mla_fwd_pools_at -- kpool_sparse_mla_fwd_pools for positioned
+ * queries (decode, chunked prefill): J(t) is what kpool_expand_indices_at
+ * would write; kv holds the Tk key tokens indexed by cu_seqlens_k.
+ */
+KPOOL_API int kpool_sparse_mla_fwd_pools_at(const void *q, const void *kv, const int32_t *pool_idx,
+                                            const int32_t *cu_seqlens_q, const int32_t *q_start_pos,
+                                            const int32_t *cu_seqlens_k, const int32_t *cu_pools,
+                                            int n_docs, int64_t Tq, int64_t Tk, int H, int Dc,
+                                            int kpool, int index_topk, int always_select_tail,
+                                            float softmax_scale, void *o_out, float *lse_out,
+                                            void *workspace, size_t workspace_bytes,
+                                            kpool_stream_t stream);
+
+/*
  * kpool_read_status -- debug helper: synchronously copy the device status
  * word of a workspace (KPOOL_STATUS_* bits, 0 = clean) to *status_out.
  * Synchronises the whole device.
@@ -399,7 +465,8 @@ KPOOL_API int kpool_read_status(const void *workspace, int *status_out);
 /*
  * kpool_debug_set_wait_limit_ns -- test entry: the time limit of each wait
  * inside the scoring kernel (kpool_score_topk, _at, _noalloc, _dense and the
- * host-buffer pass) for launches made after this call, process-wide; ns = 0
+ * host-buffer pass) and the sparse attention (kpool_sparse_mla_*) for
+ * launches made after this call, process-wide; ns = 0
  * restores the default of 2 s.  Returns the previous limit.  A wait that
  * runs out sets KPOOL_STATUS_TIMEOUT in the call's status word and raises an
  * abort flag in its CTA: the CTA's roles stop waiting, let their in-flight

@@ -56,6 +56,13 @@ _SIGS = {
     "kpool_score_topk_at": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I, _I,
                                  _P, _P, _P, _SZ, _P]),
     "kpool_expand_indices_at": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _P, _P]),
+    "kpool_sparse_mla_workspace_size": (_SZ, []),
+    "kpool_sparse_mla_fwd": (_I, [_P, _P, _P, _L, _L, _I, _I, _I, ctypes.c_float, _P, _P, _P,
+                                  _SZ, _P]),
+    "kpool_sparse_mla_fwd_pools": (_I, [_P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _I, _I,
+                                        ctypes.c_float, _P, _P, _P, _SZ, _P]),
+    "kpool_sparse_mla_fwd_pools_at": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _L, _L, _I, _I, _I,
+                                           _I, _I, ctypes.c_float, _P, _P, _P, _SZ, _P]),
     "kpool_read_status": (_I, [_P, _P]),
     "kpool_score_topk_noalloc_status": (_I, [_P]),
     "kpool_debug_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -361,6 +368,79 @@ def kpool_expand_indices_at(pool_idx, kpool: int, index_topk: int, cu_seqlens_q,
                                         _ptr(tok), _stream(pool_idx.device)),
            "kpool_expand_indices_at")
     return tok
+
+
+def kpool_sparse_mla_workspace_size() -> int:
+    return int(_lib.kpool_sparse_mla_workspace_size())
+
+
+def _mla_outputs(q, workspace, o, lse):
+    T, H, Dc = q.shape
+    if o is None:
+        o = torch.empty(T, H, Dc, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(T, H, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(kpool_sparse_mla_workspace_size(), dtype=torch.uint8,
+                                device=q.device)
+    return o, lse, workspace
+
+
+def kpool_sparse_mla_fwd(q, kv, tok_idx, softmax_scale: float, workspace=None, o=None, lse=None):
+    """Sparse attention over explicit token lists: q bf16 [T, 64, 512], kv bf16
+    [Tk, 512], tok_idx int32 [T, W] (-1 = none) -> (o bf16 [T, 64, 512], lse
+    fp32 [T, 64])."""
+    _need(q, "q", torch.bfloat16)
+    _need(kv, "kv", torch.bfloat16)
+    _need(tok_idx, "tok_idx", torch.int32)
+    T, H, Dc = q.shape
+    o, lse, workspace = _mla_outputs(q, workspace, o, lse)
+    _check(_lib.kpool_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(tok_idx), T, kv.shape[0],
+                                     tok_idx.shape[1], H, Dc, float(softmax_scale), _ptr(o),
+                                     _ptr(lse), _ptr(workspace), workspace.numel(),
+                                     _stream(q.device)), "kpool_sparse_mla_fwd")
+    return o, lse
+
+
+def kpool_sparse_mla_fwd_pools(q, kv, pool_idx, kpool: int, index_topk: int,
+                               softmax_scale: float, cu_seqlens=None, cu_pools=None,
+                               always_select_tail: bool = True, workspace=None, o=None, lse=None):
+    """Sparse attention fused with the expansion of pool_idx [T, index_topk //
+    kpool] (keys = the query tokens, kv bf16 [T, 512])."""
+    _need(q, "q", torch.bfloat16)
+    _need(kv, "kv", torch.bfloat16)
+    _need(pool_idx, "pool_idx", torch.int32)
+    n_docs = _docs(cu_seqlens, cu_pools)
+    T, H, Dc = q.shape
+    o, lse, workspace = _mla_outputs(q, workspace, o, lse)
+    _check(_lib.kpool_sparse_mla_fwd_pools(_ptr(q), _ptr(kv), _ptr(pool_idx), _ptr(cu_seqlens),
+                                           _ptr(cu_pools), n_docs, T, H, Dc, kpool, index_topk,
+                                           int(bool(always_select_tail)), float(softmax_scale),
+                                           _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                           _stream(q.device)), "kpool_sparse_mla_fwd_pools")
+    return o, lse
+
+
+def kpool_sparse_mla_fwd_pools_at(q, kv, pool_idx, kpool: int, index_topk: int,
+                                  softmax_scale: float, cu_seqlens_q, q_start_pos, cu_seqlens_k,
+                                  cu_pools, always_select_tail: bool = True, workspace=None,
+                                  o=None, lse=None):
+    """kpool_sparse_mla_fwd_pools for positioned queries (keys kv [Tk, 512])."""
+    _need(q, "q", torch.bfloat16)
+    _need(kv, "kv", torch.bfloat16)
+    _need(pool_idx, "pool_idx", torch.int32)
+    for t_, n_ in ((cu_seqlens_q, "cu_seqlens_q"), (q_start_pos, "q_start_pos"),
+                   (cu_seqlens_k, "cu_seqlens_k"), (cu_pools, "cu_pools")):
+        _need(t_, n_, torch.int32)
+    T, H, Dc = q.shape
+    o, lse, workspace = _mla_outputs(q, workspace, o, lse)
+    _check(_lib.kpool_sparse_mla_fwd_pools_at(
+        _ptr(q), _ptr(kv), _ptr(pool_idx), _ptr(cu_seqlens_q), _ptr(q_start_pos),
+        _ptr(cu_seqlens_k), _ptr(cu_pools), cu_seqlens_q.numel() - 1, T, kv.shape[0], H, Dc,
+        kpool, index_topk, int(bool(always_select_tail)), float(softmax_scale), _ptr(o),
+        _ptr(lse), _ptr(workspace), workspace.numel(), _stream(q.device)),
+        "kpool_sparse_mla_fwd_pools_at")
+    return o, lse
 
 
 def _host_cu(cu_seqlens_host):

@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkpool.so")
 SOURCES = ["kpool_api.cu", "kpool_compress.cu", "kpool_expand.cu", "kpool_score.cu",
-           "kpool_pipeline.cu", "kpool_project.cu"]
+           "kpool_pipeline.cu", "kpool_project.cu", "kpool_mla.cu"]
 HEADERS = ["kpool_internal.h", "kpool_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

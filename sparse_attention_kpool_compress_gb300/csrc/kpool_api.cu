@@ -7,6 +7,8 @@
 #include <string>
 #include <vector>
 
+#include <cmath>
+
 #include "kpool_internal.h"
 
 namespace kpool {
@@ -76,6 +78,29 @@ int check_common(int64_t T, int kpool)
     if (T < 0 || T > 0x7FFFFFFFLL) return fail(KPOOL_ERR_INVALID_ARG, "T out of range");
     if (kpool < 1 || kpool > 64)
         return fail(KPOOL_ERR_UNSUPPORTED, "kpool must be in [1, 64] (got %d)", kpool);
+    return KPOOL_OK;
+}
+
+// Shared checks of the sparse-attention entry points.
+int check_mla_args(const void *q, const void *kv, int64_t T, int64_t Tk, int H, int Dc,
+                   float scale, const void *o_out, const float *lse_out, const void *workspace,
+                   size_t workspace_bytes)
+{
+    if (T < 0 || T > 0x7FFFFFFFLL) return fail(KPOOL_ERR_INVALID_ARG, "T out of range");
+    if (Tk < 0 || Tk > 0x7FFFFFFFLL) return fail(KPOOL_ERR_INVALID_ARG, "Tk out of range");
+    if (H != 64 || Dc != 512)
+        return fail(KPOOL_ERR_UNSUPPORTED, "the sparse attention is built for H = 64, Dc = 512 "
+                    "(got H = %d, Dc = %d)", H, Dc);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(KPOOL_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+    if (T > 0 && (!q || !o_out || !lse_out))
+        return fail(KPOOL_ERR_INVALID_ARG, "q, o_out and lse_out are required");
+    if (T > 0 && !kv) return fail(KPOOL_ERR_INVALID_ARG, "kv is required");
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(o_out, 16) || !aligned(lse_out, 4))
+        return fail(KPOOL_ERR_INVALID_ARG, "q, kv and o_out must be 16-byte aligned");
+    if (!workspace || workspace_bytes < sparse_mla_workspace_bytes() || !aligned(workspace, 256))
+        return fail(KPOOL_ERR_WORKSPACE, "workspace of at least %zu bytes, 256-byte aligned, needed",
+                    sparse_mla_workspace_bytes());
     return KPOOL_OK;
 }
 
@@ -587,5 +612,87 @@ int kpool_score_topk_noalloc_status(int *status_out)
 }
 
 uint64_t kpool_debug_set_wait_limit_ns(uint64_t ns) { return set_wait_limit_ns(ns); }
+
+size_t kpool_sparse_mla_workspace_size(void) { return sparse_mla_workspace_bytes(); }
+
+int kpool_sparse_mla_fwd(const void *q, const void *kv, const int32_t *tok_idx, int64_t T,
+                         int64_t Tk, int W, int H, int Dc, float softmax_scale, void *o_out,
+                         float *lse_out, void *workspace, size_t workspace_bytes,
+                         kpool_stream_t stream)
+{
+    clear_error();
+    KPOOL_NVTX_RANGE("kpool_sparse_mla_fwd");
+    int rc = check_mla_args(q, kv, T, Tk, H, Dc, softmax_scale, o_out, lse_out, workspace,
+                            workspace_bytes);
+    if (rc) return rc;
+    if (W < 0 || W > (1 << 20)) return fail(KPOOL_ERR_INVALID_ARG, "W out of range");
+    if (T > 0 && W > 0 && !tok_idx) return fail(KPOOL_ERR_INVALID_ARG, "tok_idx is required");
+    if (!aligned(tok_idx, 4)) return fail(KPOOL_ERR_INVALID_ARG, "tok_idx must be 4-byte aligned");
+    SparseMlaArgs a{};
+    a.q = q; a.kv = kv; a.tok_idx = tok_idx; a.T = T; a.Tk = Tk; a.W = W; a.n_docs = 1;
+    a.kpool = 1; a.scale = softmax_scale; a.o = o_out; a.lse = lse_out; a.workspace = workspace;
+    // a zero-width list still runs the kernel (every row gets o = 0 and
+    // lse = -inf); the kernel never reads a row of width 0
+    if (W == 0) a.tok_idx = static_cast<const int32_t *>(workspace);
+    return run_sparse_mla(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kpool_sparse_mla_fwd_pools(const void *q, const void *kv, const int32_t *pool_idx,
+                               const int32_t *cu_seqlens, const int32_t *cu_pools, int n_docs,
+                               int64_t T, int H, int Dc, int kpool, int index_topk,
+                               int always_select_tail, float softmax_scale, void *o_out,
+                               float *lse_out, void *workspace, size_t workspace_bytes,
+                               kpool_stream_t stream)
+{
+    clear_error();
+    KPOOL_NVTX_RANGE("kpool_sparse_mla_fwd_pools");
+    int rc = check_mla_args(q, kv, T, T, H, Dc, softmax_scale, o_out, lse_out, workspace,
+                            workspace_bytes);
+    if (rc) return rc;
+    if ((rc = check_common(T, kpool))) return rc;
+    if (index_topk < 1 || index_topk % kpool != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
+    if ((rc = check_docs(cu_seqlens, cu_pools, n_docs, T, kpool, -1))) return rc;
+    if (T > 0 && !pool_idx) return fail(KPOOL_ERR_INVALID_ARG, "pool_idx is required");
+    if (!aligned(pool_idx, 4)) return fail(KPOOL_ERR_INVALID_ARG, "pool_idx must be 4-byte aligned");
+    SparseMlaArgs a{};
+    a.q = q; a.kv = kv; a.pool_idx = pool_idx; a.cu_seqlens = cu_seqlens; a.cu_pools = cu_pools;
+    a.n_docs = n_docs; a.T = T; a.Tk = T; a.kpool = kpool; a.Kp = index_topk / kpool;
+    a.tail = always_select_tail ? 1 : 0; a.scale = softmax_scale; a.o = o_out; a.lse = lse_out;
+    a.workspace = workspace;
+    return run_sparse_mla(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kpool_sparse_mla_fwd_pools_at(const void *q, const void *kv, const int32_t *pool_idx,
+                                  const int32_t *cu_seqlens_q, const int32_t *q_start_pos,
+                                  const int32_t *cu_seqlens_k, const int32_t *cu_pools, int n_docs,
+                                  int64_t Tq, int64_t Tk, int H, int Dc, int kpool, int index_topk,
+                                  int always_select_tail, float softmax_scale, void *o_out,
+                                  float *lse_out, void *workspace, size_t workspace_bytes,
+                                  kpool_stream_t stream)
+{
+    clear_error();
+    KPOOL_NVTX_RANGE("kpool_sparse_mla_fwd_pools_at");
+    int rc = check_mla_args(q, kv, Tq, Tk, H, Dc, softmax_scale, o_out, lse_out, workspace,
+                            workspace_bytes);
+    if (rc) return rc;
+    if ((rc = check_common(Tq, kpool))) return rc;
+    if (!cu_seqlens_q || !q_start_pos || !cu_seqlens_k || !cu_pools)
+        return fail(KPOOL_ERR_INVALID_ARG,
+                    "cu_seqlens_q, q_start_pos, cu_seqlens_k and cu_pools are required");
+    if (n_docs < 1) return fail(KPOOL_ERR_INVALID_ARG, "n_docs must be >= 1");
+    if (!aligned(cu_seqlens_q, 4) || !aligned(q_start_pos, 4) || !aligned(cu_seqlens_k, 4) ||
+        !aligned(cu_pools, 4) || !aligned(pool_idx, 4))
+        return fail(KPOOL_ERR_INVALID_ARG, "index arrays must be 4-byte aligned");
+    if (index_topk < 1 || index_topk % kpool != 0)
+        return fail(KPOOL_ERR_INVALID_ARG, "index_topk must be a positive multiple of kpool");
+    if (Tq > 0 && !pool_idx) return fail(KPOOL_ERR_INVALID_ARG, "pool_idx is required");
+    SparseMlaArgs a{};
+    a.q = q; a.kv = kv; a.pool_idx = pool_idx; a.cu_seqlens = cu_seqlens_q; a.q_pos = q_start_pos;
+    a.cu_k = cu_seqlens_k; a.cu_pools = cu_pools; a.n_docs = n_docs; a.T = Tq; a.Tk = Tk;
+    a.kpool = kpool; a.Kp = index_topk / kpool; a.tail = always_select_tail ? 1 : 0;
+    a.scale = softmax_scale; a.o = o_out; a.lse = lse_out; a.workspace = workspace;
+    return run_sparse_mla(a, reinterpret_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

@@ -120,6 +120,24 @@ size_t pipeline_scratch_bytes(int64_t T, int H, int D, int n_docs, int kpool, in
                               int fp8, int64_t chunk_rows, int64_t P_total);
 int run_pipeline(const PipelineArgs &a, cudaStream_t stream);
 
+// Sparse attention over the selection (kpool_mla.cu): tok_idx mode when
+// tok_idx is given, else pool mode (the expansion of pool_idx fused in).
+struct SparseMlaArgs {
+    const void *q, *kv;                 // bf16 [T, 64, 512], bf16 [Tk, 512]
+    const int32_t *tok_idx;             // [T, W] or NULL
+    const int32_t *pool_idx;            // [T, Kp] (pool mode)
+    const int32_t *cu_seqlens, *q_pos, *cu_k, *cu_pools;
+    int n_docs;
+    int64_t T, Tk;
+    int W, kpool, Kp, tail;
+    float scale;
+    void *o;                            // bf16 [T, 64, 512]
+    float *lse;                         // [T, 64]
+    void *workspace;                    // >= sparse_mla_workspace_bytes(), 256-byte aligned
+};
+size_t sparse_mla_workspace_bytes();
+int run_sparse_mla(const SparseMlaArgs &a, cudaStream_t s);
+
 // Query tiles the fixed scratch of kpool_score_topk_noalloc can schedule.
 constexpr int kNoAllocMaxTiles = 131072;
 // Device address, size and tile capacity of the no-alloc scratch array of

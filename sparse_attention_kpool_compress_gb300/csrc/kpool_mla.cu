@@ -1,0 +1,728 @@
+// Sparse attention over the indexer's selection: the absorbed NoPE MLA
+// forward (xtuner PR "GLM-5.3-Flash F5: NoPE DSA + KPool indexer + clamped
+// SwiGLU", Summary: a FlashMLA-style SparseMLA forward over the selected token
+// indices, with 64 heads in the production config; Megatron-LM PR "GLM5.3
+// Flash (KDA + mHC + KPool DSA) support + FP8", Changes section 3, "NoPE": the
+// absorbed query has no positional slice, so scores and values both use the
+// 512-wide latent rows).  For query row t and head h, over the row's token
+// list J(t):
+//
+//   s_j = scale * q[t, h, :] . c[j, :]
+//   o[t, h, :] = sum_j softmax_j(s) c[j, :],   lse[t, h] = ln sum_j exp(s_j)
+//
+// J(t) is an explicit tok_idx row (-1 = none) or, fused with the expansion,
+// the row's selected pools (kpool consecutive tokens each) plus its causal
+// tail, computed on the fly so that the token table never reaches memory.
+//
+// Design (one persistent CTA per SM, 8 warps, rows handed out by an atomic
+// counter):
+//   warps 0, 2  loaders: the row's 64 x 512 query block, then per block of
+//               128 listed tokens their latent rows, gathered with 16-byte
+//               cp.async into 128-byte-swizzled tiles (4 slots of 128 tokens
+//               x 128 latent columns make one block); warp 0 also publishes a
+//               record per block (row, block, token-validity mask)
+//   warp 1      TMEM allocation and the tcgen05.mma issuer (one thread)
+//   warps 4-7   online softmax and output, one TMEM lane per thread (a
+//               listed token for the scores, a latent column for the output)
+// Both contractions run transposed, so every MMA has M = 128 and the 64
+// heads are its N dimension:
+//   S^T [128 tokens x 64 heads]   = C_blk [128 x 512] . Q^T          (A, B K-major)
+//   O^T [512 latent x 64 heads]  += C_blk^T [512 x 128] . P^T        (A MN-major)
+// S^T is double-buffered in TMEM (2 x 64 columns) and O^T takes 4 x 64.  The
+// online softmax keeps one reference maximum m per head and rescales O^T in
+// TMEM only when a block's score exceeds m by more than 8 in the base-2
+// exponent; P = 2^(s*scale*log2(e) - m) <= 256 goes to shared memory in BF16.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "kpool_internal.h"
+#include "kpool_ptx.cuh"
+
+namespace kpool {
+namespace {
+
+constexpr int kH = 64;                  // heads = MMA N
+constexpr int kDc = 512;                // latent width
+constexpr int kBT = 128;                // listed tokens per block = MMA M of S^T
+constexpr int kThreads = 256;
+constexpr int kLoaders = 64;            // warps 0 and 2
+constexpr int kSmThreads = 128;         // warps 4..7
+constexpr int kRowBytes = kDc * 2;      // 1024 bytes of one latent row / query head
+constexpr int kChunk = kBT * 128;       // one 64-column chunk of a block: 16 KiB
+constexpr int kSlotBytes = 2 * kChunk;  // one slot: 128 latent columns of a block
+constexpr int kSlots = 4;
+constexpr int kQChunk = kH * 128;       // 64 latent columns of the query block: 8 KiB
+constexpr float kRescale = 8.f;         // headroom of the reference maximum (log2)
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr int kTmemCols = 512;          // S^T: 0..127, O^T: 128..383
+
+// shared memory (from a 1024-byte aligned base)
+constexpr int kOffC = 0;
+constexpr int kOffQ = kOffC + kSlots * kSlotBytes;   // 131072
+constexpr int kOffP = kOffQ + 8 * kQChunk;           // 196608
+constexpr int kOffRed = kOffP + 2 * kQChunk;         // 212992: [4][64] floats
+constexpr int kOffM = kOffRed + 4 * kH * 4;          // reference maxima [64]
+constexpr int kOffL = kOffM + kH * 4;                // per-head scratch [64]
+constexpr int kOffFlag = kOffL + kH * 4;             // agreement words [2][4]
+constexpr int kOffRow = kOffFlag + 32;               // RowMsg [2]
+constexpr int kOffInfo = kOffRow + 2 * 48;           // BInfo [2]
+constexpr int kOffBar = kOffInfo + 2 * 32;
+enum {
+    BQ_FULL = 0, BQ_EMPTY, BC_FULL, BC_EMPTY = BC_FULL + kSlots, BS_FULL = BC_EMPTY + kSlots,
+    BS_EMPTY = BS_FULL + 2, BP_FULL = BS_EMPTY + 2, BO_FULL, BO_EMPTY, BI_FULL,
+    BI_EMPTY = BI_FULL + 2, BDRAIN = BI_EMPTY + 2, NBARS
+};
+constexpr int kOffMisc = kOffBar + NBARS * 8;        // [0] tmem base, [1] abort flag
+constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;         // alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
+
+struct Params {
+    const uint16_t *q;          // bf16 [T, 64, 512]
+    const uint16_t *kv;         // bf16 [Tk, 512]
+    const int32_t *tok;         // [T, W] or NULL (pool mode)
+    const int32_t *pool_idx;    // [T, Kp] (pool mode)
+    const int32_t *cu_seqlens, *q_pos, *cu_k, *cu_pools;
+    int n_docs;
+    int T, Tk, W, kp, Kp, tail;
+    float c_scale;              // softmax scale * log2(e)
+    uint16_t *o;                // bf16 [T, 64, 512]
+    float *lse;                 // [T, 64]
+    int *ws;                    // [0] row counter, [1] status
+    uint64_t wait_limit_ns;
+};
+
+// What the loaders need to list the tokens of one row.
+struct RowMsg {
+    int64_t key0;               // first key token of the row's document
+    int t, n_slots, tau, pool_lo, pool_hi, n_sel, n_tail, pad;
+};
+static_assert(sizeof(RowMsg) <= 48, "RowMsg slot");
+
+// One block of a row, for the MMA issuer and the softmax warps.
+struct BInfo {
+    int t, b, nb, ksteps;
+    uint32_t mask[4];           // bit r of mask[r / 32]: listed token r is valid
+};
+static_assert(sizeof(BInfo) == 32, "BInfo slot");
+
+struct Sync {
+    volatile uint32_t *abort_flag;
+    int *status;
+    uint64_t limit_ns;
+};
+
+// Bounded mbarrier wait (completion, then the CTA abort flag, then a timer
+// that raises the flag and KPOOL_STATUS_TIMEOUT).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sync &sy)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*sy.abort_flag) return false;
+        if (ptx::globaltimer() - t0 > sy.limit_ns) {
+            *sy.abort_flag = 1u;
+            atomicOr(sy.status, KPOOL_STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Sync &sy)
+{
+    const bool ok = wait_bar(bar, parity, sy);
+    return __all_sync(kFull, ok);
+}
+
+// Document of row t (largest d with cu[d] <= t), one warp probing 32 evenly
+// spaced offsets per round.  Every lane gets the answer.
+__device__ __forceinline__ int doc_of_row(const int32_t *cu, int n_docs, int t, int lane)
+{
+    int lo = 0, hi = n_docs;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = lo + lane * step;
+        const bool le = idx < hi && cu[idx] <= t;
+        const unsigned m = __ballot_sync(kFull, le);
+        const int nlo = lo + (31 - __clz(m)) * step;
+        hi = min(hi, nlo + step);
+        lo = nlo;
+    }
+    return lo;
+}
+
+// Key token of slot j of the row (-1: none).  Pool mode lists the selected
+// pools' tokens in order, then the tail (the expansion of the selection).
+__device__ __forceinline__ int token_of(const Params &p, const RowMsg &m, int j)
+{
+    if (j >= m.n_slots) return -1;
+    if (p.tok != nullptr) {
+        const int v = __ldg(p.tok + static_cast<int64_t>(m.t) * p.W + j);
+        return (v >= 0 && v < p.Tk) ? v : -1;
+    }
+    const int npt = m.n_sel * p.kp;
+    int64_t v = -1;
+    if (j < npt) {
+        const int e = j / p.kp;
+        const int g = __ldg(p.pool_idx + static_cast<int64_t>(m.t) * p.Kp + e);
+        if (g >= m.pool_lo && g < m.pool_hi)
+            v = m.key0 + static_cast<int64_t>(g - m.pool_lo) * p.kp + (j - e * p.kp);
+    } else {
+        v = m.key0 + m.tau - m.n_tail + 1 + (j - npt);
+    }
+    return (v >= 0 && v < p.Tk) ? static_cast<int>(v) : -1;
+}
+
+// Warp 0: the next row's message (t = -1 when there is none or on abort).
+__device__ RowMsg next_row(const Params &p, int lane, bool go)
+{
+    RowMsg m{};
+    int t = -1;
+    if (lane == 0 && go) t = atomicAdd(p.ws, 1);
+    t = __shfl_sync(kFull, t, 0);
+    m.t = (t >= 0 && t < p.T) ? t : -1;
+    if (m.t < 0) return m;
+    if (p.tok != nullptr) {
+        // extent of the listed tokens: one past the last valid entry
+        int last = -1;
+        const int32_t *row = p.tok + static_cast<int64_t>(m.t) * p.W;
+        for (int j = lane; j < p.W; j += 32) {
+            const int v = __ldg(row + j);
+            if (v >= 0 && v < p.Tk) last = j;
+        }
+        m.n_slots = __reduce_max_sync(kFull, last + 1);
+        return m;
+    }
+    int64_t doc_start = 0;
+    m.key0 = 0;
+    int pos0 = 0;
+    m.pool_lo = 0;
+    m.pool_hi = p.Tk / p.kp;
+    if (p.cu_seqlens != nullptr) {
+        const int d = doc_of_row(p.cu_seqlens, p.n_docs, m.t, lane);
+        doc_start = p.cu_seqlens[d];
+        m.key0 = p.cu_k != nullptr ? p.cu_k[d] : doc_start;
+        pos0 = p.q_pos != nullptr ? p.q_pos[d] : 0;
+        m.pool_lo = p.cu_pools[d];
+        m.pool_hi = p.cu_pools[d + 1];
+    }
+    m.tau = pos0 + static_cast<int>(m.t - doc_start);
+    const int nc = min((m.tau + 1) / p.kp, m.pool_hi - m.pool_lo);
+    m.n_sel = max(0, min(nc, p.Kp));
+    m.n_tail = p.tail ? (m.tau + 1) % p.kp : 0;
+    m.n_slots = m.n_sel * p.kp + m.n_tail;
+    return m;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t sC = sbase + kOffC, sQ = sbase + kOffQ, sP = sbase + kOffP;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    RowMsg *rows_s = reinterpret_cast<RowMsg *>(smem + kOffRow);
+    BInfo *info = reinterpret_cast<BInfo *>(smem + kOffInfo);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(BQ_FULL), kLoaders);
+        ptx::mbar_init(bar(BQ_EMPTY), 1);
+        for (int i = 0; i < kSlots; ++i) {
+            ptx::mbar_init(bar(BC_FULL + i), kLoaders);
+            ptx::mbar_init(bar(BC_EMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(bar(BS_FULL + i), 1);
+            ptx::mbar_init(bar(BS_EMPTY + i), 4);
+            ptx::mbar_init(bar(BI_FULL + i), 1);
+            ptx::mbar_init(bar(BI_EMPTY + i), 1 + 4);
+        }
+        ptx::mbar_init(bar(BP_FULL), 4);
+        ptx::mbar_init(bar(BO_FULL), 1);
+        ptx::mbar_init(bar(BO_EMPTY), 4);
+        ptx::mbar_init(bar(BDRAIN), 1);
+        misc[1] = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&misc[0]), kTmemCols);
+        ptx::tmem_relinquish();
+        ptx::tc_fence_before();
+    }
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const Sync sy{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.ws + 1, p.wait_limit_ns};
+
+    if (warp == 0 || warp == 2) {
+        // ---------------- loaders ----------------
+        const int lt = (warp == 0 ? 0 : 32) + lane;   // 0..63
+        const char *kvb = reinterpret_cast<const char *>(p.kv);
+        // barriers of committed cp.async groups not yet signalled (oldest first)
+        uint32_t pend0 = 0, pend1 = 0, pend2 = 0;
+        int npend = 0;
+        auto push = [&](uint32_t b) {
+            if (npend == 0) pend0 = b;
+            else if (npend == 1) pend1 = b;
+            else pend2 = b;
+            ++npend;
+            if (npend > 2) {   // keep two groups in flight
+                ptx::cp_async_wait_group<2>();
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(pend0);
+                pend0 = pend1;
+                pend1 = pend2;
+                --npend;
+            }
+        };
+        auto flush = [&]() {
+            if (npend == 0) return;
+            ptx::cp_async_wait_all();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(pend0);
+            if (npend > 1) ptx::mbar_arrive(pend1);
+            if (npend > 2) ptx::mbar_arrive(pend2);
+            npend = 0;
+        };
+        // a free buffer; completed copies are signalled before blocking, since
+        // the consumer may need them to free it
+        auto acquire = [&](uint32_t b, uint32_t parity) {
+            if (ptx::mbar_try_wait(b, parity)) return true;
+            flush();
+            return wait_bar(b, parity, sy);
+        };
+        bool ok = true;
+        int blk = 0;
+        uint32_t q_ph = 0, c_ph = 0;
+        for (int it = 0;; ++it) {
+            RowMsg *rm = rows_s + (it & 1);
+            if (warp == 0) {
+                const RowMsg m = next_row(p, lane, ok && !*sy.abort_flag);
+                if (lane == 0) *rm = m;
+            }
+            ptx::named_bar_sync(2, kLoaders);
+            const RowMsg m = *rm;
+            if (m.t < 0) break;   // same value in both warps
+            const int nb = max(1, (m.n_slots + kBT - 1) / kBT);
+            // the query block: head h row of 1024 bytes, 16-byte piece lt
+            if (ok && acquire(bar(BQ_EMPTY), q_ph ^ 1)) {
+                const char *src = reinterpret_cast<const char *>(p.q) +
+                                  static_cast<int64_t>(m.t) * kH * kRowBytes + lt * 16;
+                const uint32_t dst0 = sQ + (lt >> 3) * kQChunk;
+#pragma unroll 8
+                for (int h = 0; h < kH; ++h)
+                    ptx::cp_async16(dst0 + h * 128 + (((lt & 7) ^ (h & 7)) << 4),
+                                    src + h * kRowBytes, 16u);
+                ptx::cp_async_commit();
+                push(bar(BQ_FULL));
+            } else {
+                ok = false;
+            }
+            q_ph ^= 1;
+            for (int b = 0; b < nb; ++b, ++blk) {
+                const int bs = blk & 1;
+                const uint32_t bph = (blk >> 1) & 1;
+                if (warp == 0) {
+                    uint32_t mk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        mk[i] = __ballot_sync(kFull, token_of(p, m, b * kBT + 32 * i + lane) >= 0);
+                    const bool got = __all_sync(kFull, ok && acquire(bar(BI_EMPTY + bs), bph ^ 1));
+                    if (lane == 0) {
+                        if (got) {
+                            BInfo in;
+                            in.t = m.t;
+                            in.b = b;
+                            in.nb = nb;
+                            const int n_in = max(0, min(kBT, m.n_slots - b * kBT));
+                            in.ksteps = max(1, (n_in + 15) / 16);
+                            for (int i = 0; i < 4; ++i) in.mask[i] = mk[i];
+                            info[bs] = in;
+                            ptx::mbar_arrive(bar(BI_FULL + bs));
+                        } else {
+                            ok = false;
+                        }
+                    }
+                    ok = got;
+                }
+                // this thread's 32 token rows of the block: r = lt / 16 + 4 s
+                int tokv[32];
+#pragma unroll
+                for (int s = 0; s < 32; ++s) tokv[s] = token_of(p, m, b * kBT + (lt >> 4) + 4 * s);
+                const int k = lt & 15;   // 16-byte piece of the slot's 256 latent bytes
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    if (!ok || !acquire(bar(BC_EMPTY + sl), c_ph ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst0 = sC + sl * kSlotBytes + (k >> 3) * kChunk;
+                    const int64_t col = static_cast<int64_t>(sl) * 256 + k * 16;
+#pragma unroll
+                    for (int s = 0; s < 32; ++s) {
+                        const int r = (lt >> 4) + 4 * s;
+                        const int tk = tokv[s];
+                        const char *src = tk >= 0 ? kvb + static_cast<int64_t>(tk) * kRowBytes + col : kvb;
+                        ptx::cp_async16(dst0 + r * 128 + (((k & 7) ^ (r & 7)) << 4), src,
+                                        tk >= 0 ? 16u : 0u);
+                    }
+                    ptx::cp_async_commit();
+                    push(bar(BC_FULL + sl));
+                }
+                c_ph ^= 1;
+            }
+        }
+        flush();
+        // end of the row stream for the MMA issuer and the softmax warps
+        if (warp == 0 && lane == 0) {
+            const int bs = blk & 1;
+            const uint32_t bph = (blk >> 1) & 1;
+            if (wait_bar(bar(BI_EMPTY + bs), bph ^ 1, sy)) {
+                BInfo in{};
+                in.t = -1;
+                info[bs] = in;
+                ptx::mbar_arrive(bar(BI_FULL + bs));
+            }
+        }
+        ptx::cp_async_wait_all();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = ptx::make_idesc(1u, kBT, kH);
+            constexpr uint32_t idesc_pv = idesc_qk | ptx::kIdescAMajorMN;
+            int blk = 0;
+            uint32_t q_ph = 0, c_ph = 0, p_ph = 0, o_ph = 0;
+            bool any = false;
+            for (;;) {
+                const int bs = blk & 1;
+                const uint32_t bph = (blk >> 1) & 1;
+                if (!wait_bar(bar(BI_FULL + bs), bph, sy)) break;
+                const BInfo in = info[bs];
+                ptx::mbar_arrive(bar(BI_EMPTY + bs));
+                if (in.t < 0) break;
+                if (in.b == 0) {
+                    if (!wait_bar(bar(BQ_FULL), q_ph, sy)) break;
+                    q_ph ^= 1;
+                }
+                if (!wait_bar(bar(BS_EMPTY + bs), bph ^ 1, sy)) break;
+                ptx::tc_fence_after();
+                bool ok = true;
+                // S^T = C_blk . Q^T over the 512 latent columns
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    if (!wait_bar(bar(BC_FULL + sl), c_ph, sy)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t ad = ptx::smem_desc_sw128(sC + sl * kSlotBytes + h * kChunk);
+                        const uint64_t bd = ptx::smem_desc_sw128(sQ + (2 * sl + h) * kQChunk);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            ptx::mma_bf16(tmem + bs * kH, ad + kk * 2, bd + kk * 2, idesc_qk,
+                                          (sl | h | kk) != 0);
+                    }
+                    any = true;
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar(BS_FULL + bs));
+                const bool last = in.b == in.nb - 1;
+                if (last) ptx::mma_commit(bar(BQ_EMPTY));
+                if (!wait_bar(bar(BP_FULL), p_ph, sy)) break;
+                p_ph ^= 1;
+                if (in.b == 0 && !wait_bar(bar(BO_EMPTY), o_ph ^ 1, sy)) break;
+                ptx::tc_fence_after();
+                // O^T += C_blk^T . P^T, 128 latent columns per slot
+                for (int sl = 0; sl < kSlots; ++sl) {
+                    const uint32_t a0 = sC + sl * kSlotBytes;
+                    for (int kk = 0; kk < in.ksteps; ++kk) {
+                        const uint64_t ad = ptx::smem_desc_mn_sw128(a0 + kk * 2048, kChunk);
+                        const uint64_t bd = ptx::smem_desc_sw128(sP + (kk >> 2) * kQChunk) + (kk & 3) * 2;
+                        ptx::mma_bf16(tmem + 128 + sl * kH, ad, bd, idesc_pv, (in.b > 0 || kk > 0));
+                    }
+                    ptx::mma_commit(bar(BC_EMPTY + sl));
+                }
+                c_ph ^= 1;
+                if (last) {
+                    ptx::mma_commit(bar(BO_FULL));
+                    o_ph ^= 1;
+                }
+                ++blk;
+            }
+            if (any) {
+                ptx::mma_commit(bar(BDRAIN));
+                const uint64_t t0 = ptx::globaltimer();
+                while (!ptx::mbar_try_wait(bar(BDRAIN), 0))
+                    if (ptx::globaltimer() - t0 > kTimeoutNs) break;
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------- softmax and output ----------------
+        const int sub = warp & 3;                  // TMEM lane quarter
+        const int r = 32 * sub + lane;             // listed token / latent column
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * sub) << 16);
+        float *m_s = reinterpret_cast<float *>(smem + kOffM);
+        float *red = reinterpret_cast<float *>(smem + kOffRed);
+        float *hs = reinterpret_cast<float *>(smem + kOffL);
+        volatile uint32_t *flags = reinterpret_cast<volatile uint32_t *>(smem + kOffFlag);
+        uint8_t *Pb = smem + kOffP;
+        const float c = p.c_scale;
+        float l[kH];                               // this thread's partial sums per head
+        int blk = 0, agr = 0;
+        uint32_t o_ph = 0;
+        // every softmax warp passes each agreement barrier once per round and
+        // leaves the loop on the same round
+        auto agree = [&](uint32_t word) {
+            volatile uint32_t *f = flags + (agr & 1) * 4;
+            if (lane == 0) f[sub] = word;
+            ptx::named_bar_sync(3, kSmThreads);
+            const uint32_t all = f[0] | f[1] | f[2] | f[3];
+            ++agr;
+            return all;
+        };
+        // transpose-reduce of 64 per-head values over the warp: lane ends with
+        // heads 2*lane and 2*lane + 1
+        auto warp_reduce = [&](float (&v)[kH], bool is_max) {
+#pragma unroll
+            for (int w = 16, n = 32; w >= 1; w >>= 1, n >>= 1) {
+                const bool up = (lane & w) != 0;
+#pragma unroll
+                for (int i = 0; i < n; ++i) {
+                    const float send = up ? v[i] : v[i + n];
+                    const float keep = up ? v[i + n] : v[i];
+                    const float got = __shfl_xor_sync(kFull, send, w);
+                    v[i] = is_max ? fmaxf(keep, got) : keep + got;
+                }
+            }
+        };
+        // the reference maxima (shared, read as broadcasts)
+        auto load_m = [&](float (&mr)[kH]) {
+            const float4 *m4 = reinterpret_cast<const float4 *>(m_s);
+#pragma unroll
+            for (int i = 0; i < kH / 4; ++i) {
+                const float4 x = m4[i];
+                mr[4 * i] = x.x;
+                mr[4 * i + 1] = x.y;
+                mr[4 * i + 2] = x.z;
+                mr[4 * i + 3] = x.w;
+            }
+        };
+        auto load_s = [&](int bs, float (&v)[kH]) {
+            uint32_t a[32], b2[32];
+            ptx::tmem_ld32(lane_base + bs * kH, a);
+            ptx::tmem_ld32(lane_base + bs * kH + 32, b2);
+            ptx::tmem_ld_wait2(a, b2);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                v[i] = __uint_as_float(a[i]);
+                v[32 + i] = __uint_as_float(b2[i]);
+            }
+        };
+        for (;;) {
+            const int bs = blk & 1;
+            const uint32_t bph = (blk >> 1) & 1;
+            bool ok = wait_bar_warp(bar(BI_FULL + bs), bph, sy);
+            BInfo in{};
+            in.t = -1;
+            if (ok) in = info[bs];
+            __syncwarp();
+            if (ok && lane == 0) ptx::mbar_arrive(bar(BI_EMPTY + bs));
+            const bool end = ok && in.t < 0;
+            const bool valid = ok && !end && ((in.mask[sub] >> lane) & 1u);
+            bool need = false;
+            if (ok && !end) {
+                ok = wait_bar_warp(bar(BS_FULL + bs), bph, sy);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    if (in.b == 0) {
+                        need = true;   // a new row: the reference maxima start over
+#pragma unroll
+                        for (int h = 0; h < kH; ++h) l[h] = 0.f;
+                    } else {
+                        float v[kH], mr[kH];
+                        load_s(bs, v);
+                        load_m(mr);
+#pragma unroll
+                        for (int h = 0; h < kH; ++h) need |= fmaf(v[h], c, -mr[h]) > kRescale;
+                        need = need && valid;
+                    }
+                }
+            }
+            const uint32_t all = agree((ok ? 0u : 1u) | (end ? 2u : 0u) |
+                                       (__any_sync(kFull, need) ? 4u : 0u));
+            if (all & 3u) break;
+            if (all & 4u) {
+                // exact block maximum per head, new reference maxima, rescale
+                float v[kH];
+                load_s(bs, v);
+#pragma unroll
+                for (int h = 0; h < kH; ++h) v[h] = valid ? v[h] * c : -INFINITY;
+                warp_reduce(v, true);
+                red[sub * kH + 2 * lane] = v[0];
+                red[sub * kH + 2 * lane + 1] = v[1];
+                ptx::named_bar_sync(3, kSmThreads);
+                if (sub == 0) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = 2 * lane + e;
+                        const float bm = fmaxf(fmaxf(red[h], red[kH + h]),
+                                               fmaxf(red[2 * kH + h], red[3 * kH + h]));
+                        const float mo = in.b == 0 ? -INFINITY : m_s[h];
+                        const float mn = fmaxf(mo, bm);
+                        hs[h] = (mn == -INFINITY) ? 1.f : ptx::ex2_approx(mo - mn);
+                        m_s[h] = mn;
+                    }
+                }
+                ptx::named_bar_sync(3, kSmThreads);
+                if (in.b > 0) {
+                    bool scale_o = false;
+#pragma unroll
+                    for (int h = 0; h < kH; ++h) {
+                        const float a = hs[h];
+                        l[h] *= a;
+                        scale_o |= a != 1.f;
+                    }
+                    if (scale_o) {
+                        // every PV MMA of the earlier blocks has completed (their
+                        // completion precedes this block's scores)
+#pragma unroll 1
+                        for (int sl = 0; sl < kSlots; ++sl) {
+#pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                const uint32_t ta = lane_base + 128 + sl * kH + half * 32;
+                                uint32_t ov[32];
+                                ptx::tmem_ld32(ta, ov);
+                                ptx::tmem_ld_wait(ov);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * hs[half * 32 + i]);
+                                ptx::tmem_st32(ta, ov);
+                            }
+                        }
+                        ptx::tmem_st_wait();
+                    }
+                }
+            }
+            // probabilities: P^T[h][r] (BF16) and the partial sums
+            {
+                float v[kH], mr[kH];
+                load_s(bs, v);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BS_EMPTY + bs));
+                load_m(mr);
+                uint8_t *pr = Pb + (r >> 6) * kQChunk + (r & 7) * 2;
+                const int piece = (r & 63) >> 3;
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    const float pv = valid ? ptx::ex2_approx(fmaf(v[h], c, -mr[h])) : 0.f;
+                    l[h] += pv;
+                    *reinterpret_cast<__nv_bfloat16 *>(pr + h * 128 + ((piece ^ (h & 7)) << 4)) =
+                        __float2bfloat16_rn(pv);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BP_FULL));
+            }
+            if (in.b == in.nb - 1) {
+                // the row's output once its last PV MMAs have landed
+                const bool ok2 = wait_bar_warp(bar(BO_FULL), o_ph, sy);
+                o_ph ^= 1;
+                if (agree(ok2 ? 0u : 1u) & 1u) break;
+                ptx::tc_fence_after();
+                float v[kH];
+#pragma unroll
+                for (int h = 0; h < kH; ++h) v[h] = l[h];
+                warp_reduce(v, false);
+                red[sub * kH + 2 * lane] = v[0];
+                red[sub * kH + 2 * lane + 1] = v[1];
+                ptx::named_bar_sync(3, kSmThreads);
+                if (sub == 0) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int h = 2 * lane + e;
+                        const float L = (red[h] + red[kH + h]) + (red[2 * kH + h] + red[3 * kH + h]);
+                        hs[h] = L > 0.f ? 1.f / L : 0.f;
+                        p.lse[static_cast<int64_t>(in.t) * kH + h] =
+                            L > 0.f ? (m_s[h] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+                    }
+                }
+                ptx::named_bar_sync(3, kSmThreads);
+                uint16_t *orow = p.o + static_cast<int64_t>(in.t) * kH * kDc + r;
+#pragma unroll 1
+                for (int sl = 0; sl < kSlots; ++sl) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t ov[32];
+                        ptx::tmem_ld32(lane_base + 128 + sl * kH + half * 32, ov);
+                        ptx::tmem_ld_wait(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int h = half * 32 + i;
+                            const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(ov[i]) * hs[h]);
+                            orow[static_cast<int64_t>(h) * kDc + sl * 128] =
+                                *reinterpret_cast<const uint16_t *>(&bv);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BO_EMPTY));
+            }
+            ++blk;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t sparse_mla_workspace_bytes() { return 256; }
+
+int run_sparse_mla(const SparseMlaArgs &a, cudaStream_t s)
+{
+    if (a.T == 0) return KPOOL_OK;
+    Params p{};
+    p.q = static_cast<const uint16_t *>(a.q);
+    p.kv = static_cast<const uint16_t *>(a.kv);
+    p.tok = a.tok_idx;
+    p.pool_idx = a.pool_idx;
+    p.cu_seqlens = a.cu_seqlens;
+    p.q_pos = a.q_pos;
+    p.cu_k = a.cu_k;
+    p.cu_pools = a.cu_pools;
+    p.n_docs = a.n_docs;
+    p.T = static_cast<int>(a.T);
+    p.Tk = static_cast<int>(a.Tk);
+    p.W = a.W;
+    p.kp = a.kpool;
+    p.Kp = a.Kp;
+    p.tail = a.tail;
+    p.c_scale = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+    p.o = static_cast<uint16_t *>(a.o);
+    p.lse = a.lse;
+    p.ws = static_cast<int *>(a.workspace);
+    p.wait_limit_ns = get_wait_limit_ns();
+    KPOOL_CUDA_CHECK(cudaMemsetAsync(a.workspace, 0, 8, s));
+    KPOOL_CUDA_CHECK(cudaFuncSetAttribute(sparse_mla_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), a.T));
+    sparse_mla_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    KPOOL_CUDA_CHECK(cudaGetLastError());
+    return KPOOL_OK;
+}
+
+}  // namespace kpool

@@ -98,6 +98,42 @@ PROJECTION_WORKLOADS = {
 }
 
 
+# The sparse attention that consumes the selection (absorbed NoPE MLA): 64
+# heads and a 512-wide latent (the pages' production config once the rotary
+# slice is gone); the softmax scale is not given by the pages, 512^-0.5 is used.
+MLA_HEADS = 64
+MLA_DC = 512
+MLA_SCALE = 512 ** -0.5
+MLA_WORKLOADS = {
+    "mla_32k": Workload("mla_32k", T=32768, H=64, D=128, kpool=4, index_topk=2048,
+                        desc="Sparse attention over the indexer's selection: one sequence "
+                             "T=32768, 64 heads, latent 512, kpool=4 index_topk=2048 with the "
+                             "tail (up to 2051 tokens per query), fused expansion"),
+    "mla_thd_32k": Workload("mla_thd_32k", T=32768, H=64, D=128, kpool=4, index_topk=2048,
+                            n_docs=16, doc_len_range=(256, 4096),
+                            desc="Sparse attention over the indexer's selection, packed THD: "
+                                 "16 documents, lengths U[256,4096] rescaled to 32768 tokens, "
+                                 "64 heads, latent 512, fused expansion"),
+}
+
+
+@dataclass
+class MlaInputs:
+    q: torch.Tensor      # bf16 [T, 64, 512] absorbed queries
+    kv: torch.Tensor     # bf16 [Tk, 512] latent rows (keys and values)
+    scale: float
+
+
+def make_mla_inputs(T: int, Tk: int | None = None, seed: int = 0) -> MlaInputs:
+    """q ~ N(0, 1) then kv ~ N(0, 1), both rounded to bfloat16 (one generator
+    seeded with seed + 7919, q drawn first)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed + 7919)
+    q = _normal_bf16((T, MLA_HEADS, MLA_DC), gen)
+    kv = _normal_bf16((T if Tk is None else Tk, MLA_DC), gen)
+    return MlaInputs(q, kv, MLA_SCALE)
+
+
 def doc_lengths(wl: Workload, gen: torch.Generator) -> list:
     if wl.n_docs == 1:
         return [wl.T]
