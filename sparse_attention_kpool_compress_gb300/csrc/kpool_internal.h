@@ -1,5 +1,6 @@
 // Host-side helpers shared by the library's translation units.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
@@ -119,6 +120,11 @@ struct PipelineArgs {
 size_t pipeline_scratch_bytes(int64_t T, int H, int D, int n_docs, int kpool, int index_topk,
                               int fp8, int64_t chunk_rows, int64_t P_total);
 int run_pipeline(const PipelineArgs &a, cudaStream_t stream);
+
+// TMA descriptor of a row-major bf16 [rows, cols] tensor: boxes of 64
+// columns (128 bytes, 128-byte swizzle) x box_rows rows (kpool_project.cu).
+int encode_bf16_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                     uint32_t box_rows);
 
 // Sparse attention over the selection (kpool_mla.cu): tok_idx mode when
 // tok_idx is given, else pool mode (the expansion of pool_idx fused in).

@@ -16,11 +16,10 @@
 //
 // Design (one persistent CTA per SM, 8 warps, rows handed out by an atomic
 // counter):
-//   warps 0, 2  loaders: the row's 64 x 512 query block, then per block of
-//               128 listed tokens their latent rows, gathered with 16-byte
-//               cp.async into 128-byte-swizzled tiles (4 slots of 128 tokens
-//               x 128 latent columns make one block); warp 0 also publishes a
-//               record per block (row, block, token-validity mask)
+//   warp 0      TMA loader: the row's 64 x 512 query block (tiled loads) and,
+//               per block of 128 listed tokens, their latent rows gathered four
+//               rows per tile::gather4 load into 128-byte-swizzled tiles; it
+//               also publishes a record per block (row, block, validity mask)
 //   warp 1      TMEM allocation and the tcgen05.mma issuer (one thread)
 //   warps 4-7   online softmax and output, one TMEM lane per thread (a
 //               listed token for the scores, a latent column for the output)
@@ -28,6 +27,10 @@
 // heads are its N dimension:
 //   S^T [128 tokens x 64 heads]   = C_blk [128 x 512] . Q^T          (A, B K-major)
 //   O^T [512 latent x 64 heads]  += C_blk^T [512 x 128] . P^T        (A MN-major)
+// The latent rows of a block are gathered twice, into a ring of 64-column
+// chunks for the scores and a ring of 128-column pairs for the output, so that
+// the MMAs run in the order S(g), O(g-1), S(g+1), O(g), ...: the scores of the
+// next block overlap the softmax of this one, and the loads run ahead of both.
 // S^T is double-buffered in TMEM (2 x 64 columns) and O^T takes 4 x 64.  The
 // online softmax keeps one reference maximum m per head and rescales O^T in
 // TMEM only when a block's score exceeds m by more than 8 in the base-2
@@ -47,12 +50,13 @@ constexpr int kH = 64;                  // heads = MMA N
 constexpr int kDc = 512;                // latent width
 constexpr int kBT = 128;                // listed tokens per block = MMA M of S^T
 constexpr int kThreads = 256;
-constexpr int kLoaders = 64;            // warps 0 and 2
 constexpr int kSmThreads = 128;         // warps 4..7
-constexpr int kRowBytes = kDc * 2;      // 1024 bytes of one latent row / query head
-constexpr int kChunk = kBT * 128;       // one 64-column chunk of a block: 16 KiB
-constexpr int kSlotBytes = 2 * kChunk;  // one slot: 128 latent columns of a block
-constexpr int kSlots = 4;
+constexpr int kChunk = kBT * 128;       // 64 latent columns of a block: 16 KiB
+constexpr int kPair = 2 * kChunk;       // 128 latent columns of a block: 32 KiB
+constexpr int kKSlots = 4;              // score-side ring (chunks)
+constexpr int kVSlots = 2;              // value-side ring (pairs)
+constexpr int kInfoSlots = 4;
+constexpr int kOParts = kDc / 128;      // O^T in 128-row (latent) parts of 64 columns
 constexpr int kQChunk = kH * 128;       // 64 latent columns of the query block: 8 KiB
 constexpr float kRescale = 8.f;         // headroom of the reference maximum (log2)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -60,20 +64,21 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kTmemCols = 512;          // S^T: 0..127, O^T: 128..383
 
 // shared memory (from a 1024-byte aligned base)
-constexpr int kOffC = 0;
-constexpr int kOffQ = kOffC + kSlots * kSlotBytes;   // 131072
-constexpr int kOffP = kOffQ + 8 * kQChunk;           // 196608
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + 8 * kQChunk;           // 65536
+constexpr int kOffV = kOffK + kKSlots * kChunk;      // 131072
+constexpr int kOffP = kOffV + kVSlots * kPair;       // 196608
 constexpr int kOffRed = kOffP + 2 * kQChunk;         // 212992: [4][64] floats
 constexpr int kOffM = kOffRed + 4 * kH * 4;          // reference maxima [64]
 constexpr int kOffL = kOffM + kH * 4;                // per-head scratch [64]
 constexpr int kOffFlag = kOffL + kH * 4;             // agreement words [2][4]
-constexpr int kOffRow = kOffFlag + 32;               // RowMsg [2]
-constexpr int kOffInfo = kOffRow + 2 * 48;           // BInfo [2]
-constexpr int kOffBar = kOffInfo + 2 * 32;
+constexpr int kOffInfo = kOffFlag + 32;              // BInfo [kInfoSlots]
+constexpr int kOffBar = kOffInfo + kInfoSlots * 32;
 enum {
-    BQ_FULL = 0, BQ_EMPTY, BC_FULL, BC_EMPTY = BC_FULL + kSlots, BS_FULL = BC_EMPTY + kSlots,
-    BS_EMPTY = BS_FULL + 2, BP_FULL = BS_EMPTY + 2, BO_FULL, BO_EMPTY, BI_FULL,
-    BI_EMPTY = BI_FULL + 2, BDRAIN = BI_EMPTY + 2, NBARS
+    BQ_FULL = 0, BQ_EMPTY, BK_FULL, BK_EMPTY = BK_FULL + kKSlots, BV_FULL = BK_EMPTY + kKSlots,
+    BV_EMPTY = BV_FULL + kVSlots, BS_FULL = BV_EMPTY + kVSlots, BS_EMPTY = BS_FULL + 2,
+    BP_FULL = BS_EMPTY + 2, BP_EMPTY, BO_FULL, BO_EMPTY, BI_FULL,
+    BI_EMPTY = BI_FULL + kInfoSlots, BDRAIN = BI_EMPTY + kInfoSlots, NBARS
 };
 constexpr int kOffMisc = kOffBar + NBARS * 8;        // [0] tmem base, [1] abort flag
 constexpr int kSmemUsed = kOffMisc + 16;
@@ -218,34 +223,42 @@ __device__ RowMsg next_row(const Params &p, int lane, bool go)
     return m;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = ptx::smem_u32(smem);
-    const uint32_t sC = sbase + kOffC, sQ = sbase + kOffQ, sP = sbase + kOffP;
+    const uint32_t sQ = sbase + kOffQ, sK = sbase + kOffK, sV = sbase + kOffV, sP = sbase + kOffP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
-    RowMsg *rows_s = reinterpret_cast<RowMsg *>(smem + kOffRow);
     BInfo *info = reinterpret_cast<BInfo *>(smem + kOffInfo);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar(BQ_FULL), kLoaders);
+        ptx::mbar_init(bar(BQ_FULL), 1);
         ptx::mbar_init(bar(BQ_EMPTY), 1);
-        for (int i = 0; i < kSlots; ++i) {
-            ptx::mbar_init(bar(BC_FULL + i), kLoaders);
-            ptx::mbar_init(bar(BC_EMPTY + i), 1);
+        for (int i = 0; i < kKSlots; ++i) {
+            ptx::mbar_init(bar(BK_FULL + i), 1);
+            ptx::mbar_init(bar(BK_EMPTY + i), 1);
+        }
+        for (int i = 0; i < kVSlots; ++i) {
+            ptx::mbar_init(bar(BV_FULL + i), 1);
+            ptx::mbar_init(bar(BV_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar(BS_FULL + i), 1);
             ptx::mbar_init(bar(BS_EMPTY + i), 4);
+        }
+        for (int i = 0; i < kInfoSlots; ++i) {
             ptx::mbar_init(bar(BI_FULL + i), 1);
             ptx::mbar_init(bar(BI_EMPTY + i), 1 + 4);
         }
         ptx::mbar_init(bar(BP_FULL), 4);
+        ptx::mbar_init(bar(BP_EMPTY), 1);
         ptx::mbar_init(bar(BO_FULL), 1);
         ptx::mbar_init(bar(BO_EMPTY), 4);
         ptx::mbar_init(bar(BDRAIN), 1);
@@ -262,200 +275,173 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     const uint32_t tmem = misc[0];
     const Sync sy{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.ws + 1, p.wait_limit_ns};
 
-    if (warp == 0 || warp == 2) {
-        // ---------------- loaders ----------------
-        const int lt = (warp == 0 ? 0 : 32) + lane;   // 0..63
-        const char *kvb = reinterpret_cast<const char *>(p.kv);
-        // barriers of committed cp.async groups not yet signalled (oldest first)
-        uint32_t pend0 = 0, pend1 = 0, pend2 = 0;
-        int npend = 0;
-        auto push = [&](uint32_t b) {
-            if (npend == 0) pend0 = b;
-            else if (npend == 1) pend1 = b;
-            else pend2 = b;
-            ++npend;
-            if (npend > 2) {   // keep two groups in flight
-                ptx::cp_async_wait_group<2>();
-                ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(pend0);
-                pend0 = pend1;
-                pend1 = pend2;
-                --npend;
-            }
-        };
-        auto flush = [&]() {
-            if (npend == 0) return;
-            ptx::cp_async_wait_all();
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(pend0);
-            if (npend > 1) ptx::mbar_arrive(pend1);
-            if (npend > 2) ptx::mbar_arrive(pend2);
-            npend = 0;
-        };
-        // a free buffer; completed copies are signalled before blocking, since
-        // the consumer may need them to free it
-        auto acquire = [&](uint32_t b, uint32_t parity) {
-            if (ptx::mbar_try_wait(b, parity)) return true;
-            flush();
-            return wait_bar(b, parity, sy);
-        };
+    if (warp == 0) {
+        // ---------------- TMA loader ----------------
+        if (lane == 0) {
+            ptx::tma_prefetch_desc(&tm_q);
+            ptx::tma_prefetch_desc(&tm_kv);
+        }
         bool ok = true;
-        int blk = 0;
-        uint32_t q_ph = 0, c_ph = 0;
-        for (int it = 0;; ++it) {
-            RowMsg *rm = rows_s + (it & 1);
-            if (warp == 0) {
-                const RowMsg m = next_row(p, lane, ok && !*sy.abort_flag);
-                if (lane == 0) *rm = m;
+        int g = 0;                      // blocks published
+        int kslot = 0, vslot = 0;
+        uint32_t kph = 0, vph = 0, q_ph = 0;
+        int pv0 = 0, pv1 = 0, pv2 = 0, pv3 = 0;   // this lane's 4 rows of the previous block
+        bool have_prev = false;
+        // one ring slot: wait until it is free, announce its bytes, then every
+        // lane gathers its 4 rows (rows 4*lane .. 4*lane+3 of the tile)
+        auto take = [&](int full, int empty, uint32_t parity, uint32_t bytes) {
+            ok = ok && wait_bar_warp(bar(empty), parity, sy);
+            if (ok && lane == 0) ptx::mbar_arrive_expect_tx(bar(full), bytes);
+            __syncwarp();
+            return ok;
+        };
+        auto load_values = [&]() {      // the previous block's 4 column pairs
+            for (int pr = 0; pr < 4; ++pr) {
+                if (!take(BV_FULL + vslot, BV_EMPTY + vslot, vph ^ 1, kPair)) return;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    ptx::tma_gather4(sV + vslot * kPair + h * kChunk + lane * 512, &tm_kv,
+                                     bar(BV_FULL + vslot), 128 * pr + 64 * h, pv0, pv1, pv2, pv3);
+                if (++vslot == kVSlots) { vslot = 0; vph ^= 1; }
             }
-            ptx::named_bar_sync(2, kLoaders);
-            const RowMsg m = *rm;
-            if (m.t < 0) break;   // same value in both warps
+        };
+        for (;;) {
+            const RowMsg m = next_row(p, lane, ok && !*sy.abort_flag);
+            if (m.t < 0) break;
             const int nb = max(1, (m.n_slots + kBT - 1) / kBT);
-            // the query block: head h row of 1024 bytes, 16-byte piece lt
-            if (ok && acquire(bar(BQ_EMPTY), q_ph ^ 1)) {
-                const char *src = reinterpret_cast<const char *>(p.q) +
-                                  static_cast<int64_t>(m.t) * kH * kRowBytes + lt * 16;
-                const uint32_t dst0 = sQ + (lt >> 3) * kQChunk;
-#pragma unroll 8
-                for (int h = 0; h < kH; ++h)
-                    ptx::cp_async16(dst0 + h * 128 + (((lt & 7) ^ (h & 7)) << 4),
-                                    src + h * kRowBytes, 16u);
-                ptx::cp_async_commit();
-                push(bar(BQ_FULL));
-            } else {
-                ok = false;
-            }
+            // the query block: 8 tiles of 64 heads x 64 latent columns
+            ok = ok && wait_bar_warp(bar(BQ_EMPTY), q_ph ^ 1, sy);
             q_ph ^= 1;
-            for (int b = 0; b < nb; ++b, ++blk) {
-                const int bs = blk & 1;
-                const uint32_t bph = (blk >> 1) & 1;
-                if (warp == 0) {
-                    uint32_t mk[4];
+            if (ok && lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar(BQ_FULL), 8 * kQChunk);
+                for (int c = 0; c < 8; ++c)
+                    ptx::tma_load_2d(sQ + c * kQChunk, &tm_q, bar(BQ_FULL), 64 * c, m.t * kH);
+            }
+            for (int b = 0; b < nb && ok; ++b, ++g) {
+                int tk[4];
+                uint32_t my4 = 0;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        mk[i] = __ballot_sync(kFull, token_of(p, m, b * kBT + 32 * i + lane) >= 0);
-                    const bool got = __all_sync(kFull, ok && acquire(bar(BI_EMPTY + bs), bph ^ 1));
-                    if (lane == 0) {
-                        if (got) {
-                            BInfo in;
-                            in.t = m.t;
-                            in.b = b;
-                            in.nb = nb;
-                            const int n_in = max(0, min(kBT, m.n_slots - b * kBT));
-                            in.ksteps = max(1, (n_in + 15) / 16);
-                            for (int i = 0; i < 4; ++i) in.mask[i] = mk[i];
-                            info[bs] = in;
-                            ptx::mbar_arrive(bar(BI_FULL + bs));
-                        } else {
-                            ok = false;
-                        }
-                    }
-                    ok = got;
+                for (int k = 0; k < 4; ++k) {
+                    tk[k] = token_of(p, m, b * kBT + 4 * lane + k);
+                    my4 |= (tk[k] >= 0 ? 1u : 0u) << k;
+                    if (tk[k] < 0) tk[k] = 0;   // a readable row; the softmax masks it
                 }
-                // this thread's 32 token rows of the block: r = lt / 16 + 4 s
-                int tokv[32];
-#pragma unroll
-                for (int s = 0; s < 32; ++s) tokv[s] = token_of(p, m, b * kBT + (lt >> 4) + 4 * s);
-                const int k = lt & 15;   // 16-byte piece of the slot's 256 latent bytes
-                for (int sl = 0; sl < kSlots; ++sl) {
-                    if (!ok || !acquire(bar(BC_EMPTY + sl), c_ph ^ 1)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t dst0 = sC + sl * kSlotBytes + (k >> 3) * kChunk;
-                    const int64_t col = static_cast<int64_t>(sl) * 256 + k * 16;
-#pragma unroll
-                    for (int s = 0; s < 32; ++s) {
-                        const int r = (lt >> 4) + 4 * s;
-                        const int tk = tokv[s];
-                        const char *src = tk >= 0 ? kvb + static_cast<int64_t>(tk) * kRowBytes + col : kvb;
-                        ptx::cp_async16(dst0 + r * 128 + (((k & 7) ^ (r & 7)) << 4), src,
-                                        tk >= 0 ? 16u : 0u);
-                    }
-                    ptx::cp_async_commit();
-                    push(bar(BC_FULL + sl));
+                // validity word w (tokens 32w..32w+31) from lanes 8w..8w+7
+                uint32_t mw = my4 << (4 * (lane & 7));
+                mw |= __shfl_xor_sync(kFull, mw, 1);
+                mw |= __shfl_xor_sync(kFull, mw, 2);
+                mw |= __shfl_xor_sync(kFull, mw, 4);
+                const int is = g % kInfoSlots;
+                ok = ok && wait_bar_warp(bar(BI_EMPTY + is), ((g / kInfoSlots) & 1) ^ 1, sy);
+                if (!ok) break;
+                if ((lane & 7) == 0) info[is].mask[lane >> 3] = mw;
+                if (lane == 0) {
+                    const int n_in = max(0, min(kBT, m.n_slots - b * kBT));
+                    info[is].t = m.t;
+                    info[is].b = b;
+                    info[is].nb = nb;
+                    info[is].ksteps = max(1, (n_in + 15) / 16);
                 }
-                c_ph ^= 1;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(BI_FULL + is));
+                // this block's score-side chunks
+                for (int c = 0; c < 8; ++c) {
+                    if (!take(BK_FULL + kslot, BK_EMPTY + kslot, kph ^ 1, kChunk)) break;
+                    ptx::tma_gather4(sK + kslot * kChunk + lane * 512, &tm_kv, bar(BK_FULL + kslot),
+                                     64 * c, tk[0], tk[1], tk[2], tk[3]);
+                    if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
+                }
+                // the previous block's value-side pairs
+                if (ok && have_prev) load_values();
+                pv0 = tk[0]; pv1 = tk[1]; pv2 = tk[2]; pv3 = tk[3];
+                have_prev = true;
             }
         }
-        flush();
-        // end of the row stream for the MMA issuer and the softmax warps
-        if (warp == 0 && lane == 0) {
-            const int bs = blk & 1;
-            const uint32_t bph = (blk >> 1) & 1;
-            if (wait_bar(bar(BI_EMPTY + bs), bph ^ 1, sy)) {
-                BInfo in{};
-                in.t = -1;
-                info[bs] = in;
-                ptx::mbar_arrive(bar(BI_FULL + bs));
-            }
+        // end of the block stream for the MMA issuer and the softmax warps; it
+        // goes out before the last block's value tiles, since the issuer starts
+        // that block's output MMAs (and frees value slots) only once it has
+        // seen what follows it
+        const int is = g % kInfoSlots;
+        ok = ok && wait_bar_warp(bar(BI_EMPTY + is), ((g / kInfoSlots) & 1) ^ 1, sy);
+        if (ok && lane == 0) {
+            info[is].t = -1;
+            ptx::mbar_arrive(bar(BI_FULL + is));
         }
-        ptx::cp_async_wait_all();
+        if (ok && have_prev) load_values();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::make_idesc(1u, kBT, kH);
             constexpr uint32_t idesc_pv = idesc_qk | ptx::kIdescAMajorMN;
-            int blk = 0;
-            uint32_t q_ph = 0, c_ph = 0, p_ph = 0, o_ph = 0;
-            bool any = false;
+            int g = 0, kslot = 0, vslot = 0;
+            uint32_t kph = 0, vph = 0, q_ph = 0, p_ph = 0, o_ph = 0;
+            bool any = false, have_prev = false;
+            BInfo prev{};
+            // O^T += C_blk^T . P^T for block x (its P is complete)
+            auto values = [&](const BInfo &x) {
+                if (!wait_bar(bar(BP_FULL), p_ph, sy)) return false;
+                p_ph ^= 1;
+                if (x.b == 0 && !wait_bar(bar(BO_EMPTY), o_ph ^ 1, sy)) return false;
+                ptx::tc_fence_after();
+                for (int pr = 0; pr < 4; ++pr) {
+                    if (!wait_bar(bar(BV_FULL + vslot), vph, sy)) return false;
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = sV + vslot * kPair;
+                    for (int kk = 0; kk < x.ksteps; ++kk) {
+                        const uint64_t ad = ptx::smem_desc_mn_sw128(a0 + kk * 2048, kChunk);
+                        const uint64_t bd = ptx::smem_desc_sw128(sP + (kk >> 2) * kQChunk) + (kk & 3) * 2;
+                        ptx::mma_bf16(tmem + 128 + pr * kH, ad, bd, idesc_pv, (x.b > 0 || kk > 0));
+                    }
+                    ptx::mma_commit(bar(BV_EMPTY + vslot));
+                    if (++vslot == kVSlots) { vslot = 0; vph ^= 1; }
+                }
+                ptx::mma_commit(bar(BP_EMPTY));
+                if (x.b == x.nb - 1) {
+                    ptx::mma_commit(bar(BO_FULL));
+                    o_ph ^= 1;
+                }
+                return true;
+            };
             for (;;) {
-                const int bs = blk & 1;
-                const uint32_t bph = (blk >> 1) & 1;
-                if (!wait_bar(bar(BI_FULL + bs), bph, sy)) break;
-                const BInfo in = info[bs];
-                ptx::mbar_arrive(bar(BI_EMPTY + bs));
-                if (in.t < 0) break;
+                const int is = g % kInfoSlots;
+                if (!wait_bar(bar(BI_FULL + is), (g / kInfoSlots) & 1, sy)) break;
+                const BInfo in = info[is];
+                ptx::mbar_arrive(bar(BI_EMPTY + is));
+                if (in.t < 0) {
+                    if (have_prev) values(prev);
+                    break;
+                }
                 if (in.b == 0) {
                     if (!wait_bar(bar(BQ_FULL), q_ph, sy)) break;
                     q_ph ^= 1;
                 }
-                if (!wait_bar(bar(BS_EMPTY + bs), bph ^ 1, sy)) break;
+                const int sb = g & 1;
+                if (!wait_bar(bar(BS_EMPTY + sb), ((g >> 1) & 1) ^ 1, sy)) break;
                 ptx::tc_fence_after();
                 bool ok = true;
                 // S^T = C_blk . Q^T over the 512 latent columns
-                for (int sl = 0; sl < kSlots; ++sl) {
-                    if (!wait_bar(bar(BC_FULL + sl), c_ph, sy)) {
+                for (int c = 0; c < 8; ++c) {
+                    if (!wait_bar(bar(BK_FULL + kslot), kph, sy)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
+                    const uint64_t ad = ptx::smem_desc_sw128(sK + kslot * kChunk);
+                    const uint64_t bd = ptx::smem_desc_sw128(sQ + c * kQChunk);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint64_t ad = ptx::smem_desc_sw128(sC + sl * kSlotBytes + h * kChunk);
-                        const uint64_t bd = ptx::smem_desc_sw128(sQ + (2 * sl + h) * kQChunk);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            ptx::mma_bf16(tmem + bs * kH, ad + kk * 2, bd + kk * 2, idesc_qk,
-                                          (sl | h | kk) != 0);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_bf16(tmem + sb * kH, ad + kk * 2, bd + kk * 2, idesc_qk, (c | kk) != 0);
+                    ptx::mma_commit(bar(BK_EMPTY + kslot));
+                    if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
                     any = true;
                 }
                 if (!ok) break;
-                ptx::mma_commit(bar(BS_FULL + bs));
-                const bool last = in.b == in.nb - 1;
-                if (last) ptx::mma_commit(bar(BQ_EMPTY));
-                if (!wait_bar(bar(BP_FULL), p_ph, sy)) break;
-                p_ph ^= 1;
-                if (in.b == 0 && !wait_bar(bar(BO_EMPTY), o_ph ^ 1, sy)) break;
-                ptx::tc_fence_after();
-                // O^T += C_blk^T . P^T, 128 latent columns per slot
-                for (int sl = 0; sl < kSlots; ++sl) {
-                    const uint32_t a0 = sC + sl * kSlotBytes;
-                    for (int kk = 0; kk < in.ksteps; ++kk) {
-                        const uint64_t ad = ptx::smem_desc_mn_sw128(a0 + kk * 2048, kChunk);
-                        const uint64_t bd = ptx::smem_desc_sw128(sP + (kk >> 2) * kQChunk) + (kk & 3) * 2;
-                        ptx::mma_bf16(tmem + 128 + sl * kH, ad, bd, idesc_pv, (in.b > 0 || kk > 0));
-                    }
-                    ptx::mma_commit(bar(BC_EMPTY + sl));
-                }
-                c_ph ^= 1;
-                if (last) {
-                    ptx::mma_commit(bar(BO_FULL));
-                    o_ph ^= 1;
-                }
-                ++blk;
+                ptx::mma_commit(bar(BS_FULL + sb));
+                if (in.b == in.nb - 1) ptx::mma_commit(bar(BQ_EMPTY));
+                if (have_prev && !values(prev)) break;
+                prev = in;
+                have_prev = true;
+                ++g;
             }
             if (any) {
                 ptx::mma_commit(bar(BDRAIN));
@@ -526,15 +512,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
                 v[32 + i] = __uint_as_float(b2[i]);
             }
         };
+        bool bad = false;   // a wait of the previous round failed in this warp
         for (;;) {
             const int bs = blk & 1;
             const uint32_t bph = (blk >> 1) & 1;
-            bool ok = wait_bar_warp(bar(BI_FULL + bs), bph, sy);
+            const int is = blk % kInfoSlots;
+            bool ok = !bad && wait_bar_warp(bar(BI_FULL + is), (blk / kInfoSlots) & 1, sy);
             BInfo in{};
             in.t = -1;
-            if (ok) in = info[bs];
+            if (ok) in = info[is];
             __syncwarp();
-            if (ok && lane == 0) ptx::mbar_arrive(bar(BI_EMPTY + bs));
+            if (ok && lane == 0) ptx::mbar_arrive(bar(BI_EMPTY + is));
             const bool end = ok && in.t < 0;
             const bool valid = ok && !end && ((in.mask[sub] >> lane) & 1u);
             bool need = false;
@@ -582,7 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
                     }
                 }
                 ptx::named_bar_sync(3, kSmThreads);
-                if (in.b > 0) {
+                // the previous block's output MMAs must be complete before O^T
+                // is rescaled and before P is overwritten
+                bad = !wait_bar_warp(bar(BP_EMPTY), (blk & 1) ^ 1, sy);
+                if (in.b > 0 && !bad) {
                     bool scale_o = false;
 #pragma unroll
                     for (int h = 0; h < kH; ++h) {
@@ -594,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
                         // every PV MMA of the earlier blocks has completed (their
                         // completion precedes this block's scores)
 #pragma unroll 1
-                        for (int sl = 0; sl < kSlots; ++sl) {
+                        for (int sl = 0; sl < kOParts; ++sl) {
 #pragma unroll
                             for (int half = 0; half < 2; ++half) {
                                 const uint32_t ta = lane_base + 128 + sl * kH + half * 32;
@@ -610,9 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
                         ptx::tmem_st_wait();
                     }
                 }
+            } else {
+                bad = !wait_bar_warp(bar(BP_EMPTY), (blk & 1) ^ 1, sy);
             }
             // probabilities: P^T[h][r] (BF16) and the partial sums
-            {
+            if (!bad) {
                 float v[kH], mr[kH];
                 load_s(bs, v);
                 ptx::tc_fence_before();
@@ -634,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
             }
             if (in.b == in.nb - 1) {
                 // the row's output once its last PV MMAs have landed
-                const bool ok2 = wait_bar_warp(bar(BO_FULL), o_ph, sy);
+                const bool ok2 = !bad && wait_bar_warp(bar(BO_FULL), o_ph, sy);
                 o_ph ^= 1;
                 if (agree(ok2 ? 0u : 1u) & 1u) break;
                 ptx::tc_fence_after();
@@ -658,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
                 ptx::named_bar_sync(3, kSmThreads);
                 uint16_t *orow = p.o + static_cast<int64_t>(in.t) * kH * kDc + r;
 #pragma unroll 1
-                for (int sl = 0; sl < kSlots; ++sl) {
+                for (int sl = 0; sl < kOParts; ++sl) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t ov[32];
@@ -692,9 +685,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
 
 size_t sparse_mla_workspace_bytes() { return 256; }
 
+namespace {
+// No key at all: every row gets o = 0 and lse = -inf.
+__global__ void no_keys_kernel(float *lse, int64_t n)
+{
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        lse[i] = -INFINITY;
+}
+}  // namespace
+
 int run_sparse_mla(const SparseMlaArgs &a, cudaStream_t s)
 {
+    KPOOL_CUDA_CHECK(cudaMemsetAsync(a.workspace, 0, 8, s));
     if (a.T == 0) return KPOOL_OK;
+    if (a.Tk == 0) {
+        KPOOL_CUDA_CHECK(cudaMemsetAsync(a.o, 0, static_cast<size_t>(a.T) * kH * kDc * 2, s));
+        no_keys_kernel<<<256, 256, 0, s>>>(a.lse, a.T * kH);
+        KPOOL_CUDA_CHECK(cudaGetLastError());
+        return KPOOL_OK;
+    }
+    CUtensorMap mq, mkv;
+    int rc = encode_bf16_tmap(&mq, a.q, kDc, static_cast<uint64_t>(a.T) * kH, kH);
+    if (rc) return rc;
+    rc = encode_bf16_tmap(&mkv, a.kv, kDc, static_cast<uint64_t>(a.Tk), 1);
+    if (rc) return rc;
     Params p{};
     p.q = static_cast<const uint16_t *>(a.q);
     p.kv = static_cast<const uint16_t *>(a.kv);
@@ -716,11 +731,10 @@ int run_sparse_mla(const SparseMlaArgs &a, cudaStream_t s)
     p.lse = a.lse;
     p.ws = static_cast<int *>(a.workspace);
     p.wait_limit_ns = get_wait_limit_ns();
-    KPOOL_CUDA_CHECK(cudaMemsetAsync(a.workspace, 0, 8, s));
     KPOOL_CUDA_CHECK(cudaFuncSetAttribute(sparse_mla_kernel,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), a.T));
-    sparse_mla_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    sparse_mla_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mkv, p);
     KPOOL_CUDA_CHECK(cudaGetLastError());
     return KPOOL_OK;
 }

@@ -405,6 +405,12 @@ int launch_project_kp(const CUtensorMap &mx, const CUtensorMap &mw, const ProjPa
 
 }  // namespace
 
+int encode_bf16_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                     uint32_t box_rows)
+{
+    return encode_bf16_2d(m, base, cols, rows, box_rows);
+}
+
 int run_project_compress(const ProjectArgs &a, cudaStream_t s)
 {
     KPOOL_CUDA_CHECK(cudaMemsetAsync(a.status, 0, sizeof(int), s));
