@@ -14,15 +14,18 @@
 // the row's selected pools (kpool consecutive tokens each) plus its causal
 // tail, computed on the fly so that the token table never reaches memory.
 //
-// Design (one persistent CTA per SM, 8 warps, rows handed out by an atomic
+// Design (one persistent CTA per SM, 16 warps, rows handed out by an atomic
 // counter):
-//   warp 0      TMA loader: the row's 64 x 512 query block (tiled loads) and,
-//               per block of 128 listed tokens, their latent rows gathered four
-//               rows per tile::gather4 load into 128-byte-swizzled tiles; it
-//               also publishes a record per block (row, block, validity mask)
+//   warp 0      control: the row's 64 x 512 query block (TMA tiled loads) and,
+//               per block of 128 listed tokens, a record (row, block, validity
+//               mask) with the block's token ids in shared memory
 //   warp 1      TMEM allocation and the tcgen05.mma issuer (one thread)
 //   warps 4-7   online softmax and output, one TMEM lane per thread (a
 //               listed token for the scores, a latent column for the output)
+//   warps 8-15  loaders: the listed tokens' latent rows, gathered with 16-byte
+//               cp.async into 128-byte-swizzled tiles (a gather of 128-byte
+//               rows moves about 3x more bytes per cycle this way than with
+//               one tile::gather4 TMA load per 4 rows)
 // Both contractions run transposed, so every MMA has M = 128 and the 64
 // heads are its N dimension:
 //   S^T [128 tokens x 64 heads]   = C_blk [128 x 512] . Q^T          (A, B K-major)
@@ -49,8 +52,13 @@ namespace {
 constexpr int kH = 64;                  // heads = MMA N
 constexpr int kDc = 512;                // latent width
 constexpr int kBT = 128;                // listed tokens per block = MMA M of S^T
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kSmThreads = 128;         // warps 4..7
+constexpr int kLoaders = 256;           // warps 8..15
+constexpr int kLoaderWarps = kLoaders / 32;
+// register split (setmaxnreg): 512 threads x 128 at launch; control / MMA and
+// loader warpgroups give up most of theirs to the softmax warpgroup
+constexpr int kRegsSoftmax = 232, kRegsOther = 56;
 constexpr int kChunk = kBT * 128;       // 64 latent columns of a block: 16 KiB
 constexpr int kPair = 2 * kChunk;       // 128 latent columns of a block: 32 KiB
 constexpr int kKSlots = 4;              // score-side ring (chunks)
@@ -73,7 +81,8 @@ constexpr int kOffM = kOffRed + 4 * kH * 4;          // reference maxima [64]
 constexpr int kOffL = kOffM + kH * 4;                // per-head scratch [64]
 constexpr int kOffFlag = kOffL + kH * 4;             // agreement words [2][4]
 constexpr int kOffInfo = kOffFlag + 32;              // BInfo [kInfoSlots]
-constexpr int kOffBar = kOffInfo + kInfoSlots * 32;
+constexpr int kOffTok = kOffInfo + kInfoSlots * 32;   // token ids [kInfoSlots][128]
+constexpr int kOffBar = kOffTok + kInfoSlots * kBT * 4;
 enum {
     BQ_FULL = 0, BQ_EMPTY, BK_FULL, BK_EMPTY = BK_FULL + kKSlots, BV_FULL = BK_EMPTY + kKSlots,
     BV_EMPTY = BV_FULL + kVSlots, BS_FULL = BV_EMPTY + kVSlots, BS_EMPTY = BS_FULL + 2,
@@ -224,8 +233,7 @@ __device__ RowMsg next_row(const Params &p, int lane, bool go)
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ Params p)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -235,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     BInfo *info = reinterpret_cast<BInfo *>(smem + kOffInfo);
+    int *toks = reinterpret_cast<int *>(smem + kOffTok);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -242,11 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(BQ_FULL), 1);
         ptx::mbar_init(bar(BQ_EMPTY), 1);
         for (int i = 0; i < kKSlots; ++i) {
-            ptx::mbar_init(bar(BK_FULL + i), 1);
+            ptx::mbar_init(bar(BK_FULL + i), kLoaders);
             ptx::mbar_init(bar(BK_EMPTY + i), 1);
         }
         for (int i = 0; i < kVSlots; ++i) {
-            ptx::mbar_init(bar(BV_FULL + i), 1);
+            ptx::mbar_init(bar(BV_FULL + i), kLoaders);
             ptx::mbar_init(bar(BV_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kInfoSlots; ++i) {
             ptx::mbar_init(bar(BI_FULL + i), 1);
-            ptx::mbar_init(bar(BI_EMPTY + i), 1 + 4);
+            ptx::mbar_init(bar(BI_EMPTY + i), 1 + 4 + kLoaderWarps);
         }
         ptx::mbar_init(bar(BP_FULL), 4);
         ptx::mbar_init(bar(BP_EMPTY), 1);
@@ -275,36 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = misc[0];
     const Sync sy{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.ws + 1, p.wait_limit_ns};
 
+    if (warp < 4) {
+    ptx::setmaxnreg_dec<kRegsOther>();
     if (warp == 0) {
-        // ---------------- TMA loader ----------------
-        if (lane == 0) {
-            ptx::tma_prefetch_desc(&tm_q);
-            ptx::tma_prefetch_desc(&tm_kv);
-        }
+        // ---------------- control: rows, records, query blocks ----------------
+        if (lane == 0) ptx::tma_prefetch_desc(&tm_q);
         bool ok = true;
         int g = 0;                      // blocks published
-        int kslot = 0, vslot = 0;
-        uint32_t kph = 0, vph = 0, q_ph = 0;
-        int pv0 = 0, pv1 = 0, pv2 = 0, pv3 = 0;   // this lane's 4 rows of the previous block
-        bool have_prev = false;
-        // one ring slot: wait until it is free, announce its bytes, then every
-        // lane gathers its 4 rows (rows 4*lane .. 4*lane+3 of the tile)
-        auto take = [&](int full, int empty, uint32_t parity, uint32_t bytes) {
-            ok = ok && wait_bar_warp(bar(empty), parity, sy);
-            if (ok && lane == 0) ptx::mbar_arrive_expect_tx(bar(full), bytes);
-            __syncwarp();
-            return ok;
-        };
-        auto load_values = [&]() {      // the previous block's 4 column pairs
-            for (int pr = 0; pr < 4; ++pr) {
-                if (!take(BV_FULL + vslot, BV_EMPTY + vslot, vph ^ 1, kPair)) return;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    ptx::tma_gather4(sV + vslot * kPair + h * kChunk + lane * 512, &tm_kv,
-                                     bar(BV_FULL + vslot), 128 * pr + 64 * h, pv0, pv1, pv2, pv3);
-                if (++vslot == kVSlots) { vslot = 0; vph ^= 1; }
-            }
-        };
+        uint32_t q_ph = 0;
         for (;;) {
             const RowMsg m = next_row(p, lane, ok && !*sy.abort_flag);
             if (m.t < 0) break;
@@ -324,7 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 4; ++k) {
                     tk[k] = token_of(p, m, b * kBT + 4 * lane + k);
                     my4 |= (tk[k] >= 0 ? 1u : 0u) << k;
-                    if (tk[k] < 0) tk[k] = 0;   // a readable row; the softmax masks it
                 }
                 // validity word w (tokens 32w..32w+31) from lanes 8w..8w+7
                 uint32_t mw = my4 << (4 * (lane & 7));
@@ -334,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int is = g % kInfoSlots;
                 ok = ok && wait_bar_warp(bar(BI_EMPTY + is), ((g / kInfoSlots) & 1) ^ 1, sy);
                 if (!ok) break;
+                *reinterpret_cast<int4 *>(toks + is * kBT + 4 * lane) = make_int4(tk[0], tk[1], tk[2], tk[3]);
                 if ((lane & 7) == 0) info[is].mask[lane >> 3] = mw;
                 if (lane == 0) {
                     const int n_in = max(0, min(kBT, m.n_slots - b * kBT));
@@ -344,30 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(BI_FULL + is));
-                // this block's score-side chunks
-                for (int c = 0; c < 8; ++c) {
-                    if (!take(BK_FULL + kslot, BK_EMPTY + kslot, kph ^ 1, kChunk)) break;
-                    ptx::tma_gather4(sK + kslot * kChunk + lane * 512, &tm_kv, bar(BK_FULL + kslot),
-                                     64 * c, tk[0], tk[1], tk[2], tk[3]);
-                    if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
-                }
-                // the previous block's value-side pairs
-                if (ok && have_prev) load_values();
-                pv0 = tk[0]; pv1 = tk[1]; pv2 = tk[2]; pv3 = tk[3];
-                have_prev = true;
             }
         }
-        // end of the block stream for the MMA issuer and the softmax warps; it
-        // goes out before the last block's value tiles, since the issuer starts
-        // that block's output MMAs (and frees value slots) only once it has
-        // seen what follows it
+        // end of the block stream for every consumer
         const int is = g % kInfoSlots;
-        ok = ok && wait_bar_warp(bar(BI_EMPTY + is), ((g / kInfoSlots) & 1) ^ 1, sy);
-        if (ok && lane == 0) {
+        if (ok && wait_bar_warp(bar(BI_EMPTY + is), ((g / kInfoSlots) & 1) ^ 1, sy) && lane == 0) {
             info[is].t = -1;
             ptx::mbar_arrive(bar(BI_FULL + is));
         }
-        if (ok && have_prev) load_values();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
@@ -450,7 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ptx::globaltimer() - t0 > kTimeoutNs) break;
             }
         }
-    } else if (warp >= 4) {
+    }
+    } else if (warp < 8) {
+        ptx::setmaxnreg_inc<kRegsSoftmax>();
         // ---------------- softmax and output ----------------
         const int sub = warp & 3;                  // TMEM lane quarter
         const int r = 32 * sub + lane;             // listed token / latent column
@@ -672,6 +645,108 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++blk;
         }
+    } else {
+        ptx::setmaxnreg_dec<kRegsOther>();
+        // ---------------- loaders ----------------
+        const int lt = threadIdx.x - 256;   // 0..255
+        const char *kvb = reinterpret_cast<const char *>(p.kv);
+        // barriers of committed cp.async groups not yet signalled (oldest first)
+        uint32_t pend0 = 0, pend1 = 0, pend2 = 0;
+        int npend = 0;
+        auto push = [&](uint32_t b) {
+            if (npend == 0) pend0 = b;
+            else if (npend == 1) pend1 = b;
+            else pend2 = b;
+            ++npend;
+            if (npend > 2) {   // keep two groups in flight
+                ptx::cp_async_wait_group<2>();
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(pend0);
+                pend0 = pend1;
+                pend1 = pend2;
+                --npend;
+            }
+        };
+        auto flush = [&]() {
+            if (npend == 0) return;
+            ptx::cp_async_wait_all();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(pend0);
+            if (npend > 1) ptx::mbar_arrive(pend1);
+            if (npend > 2) ptx::mbar_arrive(pend2);
+            npend = 0;
+        };
+        // completed copies are signalled before blocking: the consumer may
+        // need them to make progress
+        auto acquire = [&](uint32_t b, uint32_t parity) {
+            if (ptx::mbar_try_wait(b, parity)) return true;
+            flush();
+            return wait_bar(b, parity, sy);
+        };
+        bool ok = true;
+        int g = 0, kslot = 0, vslot = 0, prev_is = 0;
+        uint32_t kph = 0, vph = 0;
+        bool have_prev = false;
+        // the 4 column pairs (128 latent columns each) of block slot `ts`
+        auto load_values = [&](int ts) {
+            const int *tk = toks + ts * kBT;
+            for (int pr = 0; pr < 4 && ok; ++pr) {
+                ok = acquire(bar(BV_EMPTY + vslot), vph ^ 1);
+                if (!ok) break;
+                const uint32_t dst0 = sV + vslot * kPair;
+#pragma unroll
+                for (int s8 = 0; s8 < 8; ++s8) {
+                    const int piece = lt + kLoaders * s8;   // 16 pieces per row
+                    const int r = piece >> 4, k = piece & 15;
+                    const int tok = tk[r];
+                    const char *src = tok >= 0 ? kvb + static_cast<int64_t>(tok) * (kDc * 2) + pr * 256 + k * 16 : kvb;
+                    ptx::cp_async16(dst0 + (k >> 3) * kChunk + r * 128 + (((k & 7) ^ (r & 7)) << 4), src,
+                                    tok >= 0 ? 16u : 0u);
+                }
+                ptx::cp_async_commit();
+                push(bar(BV_FULL + vslot));
+                if (++vslot == kVSlots) { vslot = 0; vph ^= 1; }
+            }
+        };
+        for (;;) {
+            const int is = g % kInfoSlots;
+            ok = ok && acquire(bar(BI_FULL + is), (g / kInfoSlots) & 1);
+            if (!ok) break;
+            const int t_in = info[is].t;
+            if (t_in < 0) {
+                if (have_prev) load_values(prev_is);
+                break;
+            }
+            // this block's score-side chunks (64 latent columns each)
+            const int *tk = toks + is * kBT;
+            for (int c = 0; c < 8 && ok; ++c) {
+                ok = acquire(bar(BK_EMPTY + kslot), kph ^ 1);
+                if (!ok) break;
+                const uint32_t dst0 = sK + kslot * kChunk;
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const int piece = lt + kLoaders * s4;   // 8 pieces per row
+                    const int r = piece >> 3, k = piece & 7;
+                    const int tok = tk[r];
+                    const char *src = tok >= 0 ? kvb + static_cast<int64_t>(tok) * (kDc * 2) + c * 128 + k * 16 : kvb;
+                    ptx::cp_async16(dst0 + r * 128 + ((k ^ (r & 7)) << 4), src, tok >= 0 ? 16u : 0u);
+                }
+                ptx::cp_async_commit();
+                push(bar(BK_FULL + kslot));
+                if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
+            }
+            // the previous block's value-side pairs, then its record is free
+            if (ok && have_prev) {
+                load_values(prev_is);
+                __syncwarp();
+                if ((lt & 31) == 0) ptx::mbar_arrive(bar(BI_EMPTY + prev_is));
+            }
+            prev_is = is;
+            have_prev = true;
+            ++g;
+        }
+        flush();
+        ptx::cp_async_wait_all();
     }
 
     __syncthreads();
@@ -705,10 +780,8 @@ int run_sparse_mla(const SparseMlaArgs &a, cudaStream_t s)
         KPOOL_CUDA_CHECK(cudaGetLastError());
         return KPOOL_OK;
     }
-    CUtensorMap mq, mkv;
-    int rc = encode_bf16_tmap(&mq, a.q, kDc, static_cast<uint64_t>(a.T) * kH, kH);
-    if (rc) return rc;
-    rc = encode_bf16_tmap(&mkv, a.kv, kDc, static_cast<uint64_t>(a.Tk), 1);
+    CUtensorMap mq;
+    const int rc = encode_bf16_tmap(&mq, a.q, kDc, static_cast<uint64_t>(a.T) * kH, kH);
     if (rc) return rc;
     Params p{};
     p.q = static_cast<const uint16_t *>(a.q);
@@ -734,7 +807,7 @@ int run_sparse_mla(const SparseMlaArgs &a, cudaStream_t s)
     KPOOL_CUDA_CHECK(cudaFuncSetAttribute(sparse_mla_kernel,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), a.T));
-    sparse_mla_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mkv, p);
+    sparse_mla_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, p);
     KPOOL_CUDA_CHECK(cudaGetLastError());
     return KPOOL_OK;
 }
