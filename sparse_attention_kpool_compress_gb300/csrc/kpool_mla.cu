@@ -56,9 +56,16 @@ constexpr int kThreads = 512;
 constexpr int kSmThreads = 128;         // warps 4..7
 constexpr int kLoaders = 256;           // warps 8..15
 constexpr int kLoaderWarps = kLoaders / 32;
-// register split (setmaxnreg): 512 threads x 128 at launch; control / MMA and
-// loader warpgroups give up most of theirs to the softmax warpgroup
+constexpr int kKPieces = kBT * 8 / kLoaders;    // 16-byte pieces per loader and score chunk
+constexpr int kVPieces = kBT * 16 / kLoaders;   // ... and per value pair
+// register split (setmaxnreg): 512 threads x 128 at launch; the control / MMA
+// and loader warpgroups give up most of theirs to the softmax warpgroup
+// (16 loader warps measured no faster than 8: the gather is bound by the
+// memory path, not by issue)
 constexpr int kRegsSoftmax = 232, kRegsOther = 56;
+static_assert(128 * kRegsOther + 128 * kRegsSoftmax + kLoaders * kRegsOther <=
+                  (65536 / kThreads) / 8 * 8 * kThreads,
+              "register split above the launch's register budget");
 constexpr int kChunk = kBT * 128;       // 64 latent columns of a block: 16 KiB
 constexpr int kPair = 2 * kChunk;       // 128 latent columns of a block: 32 KiB
 constexpr int kKSlots = 4;              // score-side ring (chunks)
@@ -648,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         ptx::setmaxnreg_dec<kRegsOther>();
         // ---------------- loaders ----------------
-        const int lt = threadIdx.x - 256;   // 0..255
+        const int lt = threadIdx.x - 256;   // 0..kLoaders-1
         const char *kvb = reinterpret_cast<const char *>(p.kv);
         // barriers of committed cp.async groups not yet signalled (oldest first)
         uint32_t pend0 = 0, pend1 = 0, pend2 = 0;
@@ -687,22 +694,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0, kslot = 0, vslot = 0, prev_is = 0;
         uint32_t kph = 0, vph = 0;
         bool have_prev = false;
-        // the 4 column pairs (128 latent columns each) of block slot `ts`
+        // the 4 column pairs (128 latent columns each) of block slot `ts`: this
+        // thread copies 16-byte piece lt % 16 of rows lt / 16 + (kLoaders / 16) s;
+        // the rows' source and destination are set up once per block
         auto load_values = [&](int ts) {
             const int *tk = toks + ts * kBT;
+            const int k = lt & 15;
+            const char *src[kVPieces];
+            uint32_t off[kVPieces], sz = 0;
+#pragma unroll
+            for (int s8 = 0; s8 < kVPieces; ++s8) {
+                const int r = (lt >> 4) + (kLoaders / 16) * s8;
+                const int tok = tk[r];
+                src[s8] = kvb + (tok >= 0 ? static_cast<int64_t>(tok) * (kDc * 2) + k * 16 : 0);
+                off[s8] = (k >> 3) * kChunk + r * 128 + (((k & 7) ^ (r & 7)) << 4);
+                sz |= (tok >= 0 ? 1u : 0u) << s8;
+            }
             for (int pr = 0; pr < 4 && ok; ++pr) {
                 ok = acquire(bar(BV_EMPTY + vslot), vph ^ 1);
                 if (!ok) break;
                 const uint32_t dst0 = sV + vslot * kPair;
 #pragma unroll
-                for (int s8 = 0; s8 < 8; ++s8) {
-                    const int piece = lt + kLoaders * s8;   // 16 pieces per row
-                    const int r = piece >> 4, k = piece & 15;
-                    const int tok = tk[r];
-                    const char *src = tok >= 0 ? kvb + static_cast<int64_t>(tok) * (kDc * 2) + pr * 256 + k * 16 : kvb;
-                    ptx::cp_async16(dst0 + (k >> 3) * kChunk + r * 128 + (((k & 7) ^ (r & 7)) << 4), src,
-                                    tok >= 0 ? 16u : 0u);
-                }
+                for (int s8 = 0; s8 < kVPieces; ++s8)
+                    ptx::cp_async16(dst0 + off[s8], src[s8] + ((sz >> s8) & 1u) * (pr * 256),
+                                    ((sz >> s8) & 1u) * 16u);
                 ptx::cp_async_commit();
                 push(bar(BV_FULL + vslot));
                 if (++vslot == kVSlots) { vslot = 0; vph ^= 1; }
@@ -717,23 +732,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (have_prev) load_values(prev_is);
                 break;
             }
-            // this block's score-side chunks (64 latent columns each)
-            const int *tk = toks + is * kBT;
-            for (int c = 0; c < 8 && ok; ++c) {
-                ok = acquire(bar(BK_EMPTY + kslot), kph ^ 1);
-                if (!ok) break;
-                const uint32_t dst0 = sK + kslot * kChunk;
+            // this block's score-side chunks (64 latent columns each): piece lt % 8
+            // of rows lt / 8 + (kLoaders / 8) s
+            {
+                const int *tk = toks + is * kBT;
+                const int k = lt & 7;
+                const char *src[kKPieces];
+                uint32_t off[kKPieces], sz = 0;
 #pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    const int piece = lt + kLoaders * s4;   // 8 pieces per row
-                    const int r = piece >> 3, k = piece & 7;
+                for (int s4 = 0; s4 < kKPieces; ++s4) {
+                    const int r = (lt >> 3) + (kLoaders / 8) * s4;
                     const int tok = tk[r];
-                    const char *src = tok >= 0 ? kvb + static_cast<int64_t>(tok) * (kDc * 2) + c * 128 + k * 16 : kvb;
-                    ptx::cp_async16(dst0 + r * 128 + ((k ^ (r & 7)) << 4), src, tok >= 0 ? 16u : 0u);
+                    src[s4] = kvb + (tok >= 0 ? static_cast<int64_t>(tok) * (kDc * 2) + k * 16 : 0);
+                    off[s4] = r * 128 + ((k ^ (r & 7)) << 4);
+                    sz |= (tok >= 0 ? 1u : 0u) << s4;
                 }
-                ptx::cp_async_commit();
-                push(bar(BK_FULL + kslot));
-                if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
+                for (int c = 0; c < 8 && ok; ++c) {
+                    ok = acquire(bar(BK_EMPTY + kslot), kph ^ 1);
+                    if (!ok) break;
+                    const uint32_t dst0 = sK + kslot * kChunk;
+#pragma unroll
+                    for (int s4 = 0; s4 < kKPieces; ++s4)
+                        ptx::cp_async16(dst0 + off[s4], src[s4] + ((sz >> s4) & 1u) * (c * 128),
+                                        ((sz >> s4) & 1u) * 16u);
+                    ptx::cp_async_commit();
+                    push(bar(BK_FULL + kslot));
+                    if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
+                }
             }
             // the previous block's value-side pairs, then its record is free
             if (ok && have_prev) {
