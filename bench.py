@@ -417,6 +417,11 @@ def run_mla(args):
     Tensor-bound: 4 * H * Dc FLOPs per (query, listed token) pair (scores and
     output), counted over the valid listed tokens."""
     wl = W.MLA_WORKLOADS[args.workload]
+    if args.T is not None:
+        from dataclasses import replace
+        if wl.n_docs > 1:
+            raise ValueError("--T applies to single-sequence workloads only")
+        wl = replace(wl, T=args.T, name="%s_T%d" % (wl.name, args.T))
     world, rank, local = dist_env()
     if args.impl == "reference":
         print(json.dumps({"impl": "reference", "unavailable": "the oracle arm covers the indexer "
