@@ -30,11 +30,14 @@
 // heads are its N dimension:
 //   S^T [128 tokens x 64 heads]   = C_blk [128 x 512] . Q^T          (A, B K-major)
 //   O^T [512 latent x 64 heads]  += C_blk^T [512 x 128] . P^T        (A MN-major)
-// The latent rows of a block are gathered twice, into a ring of 64-column
-// chunks for the scores and a ring of 128-column pairs for the output, so that
-// the MMAs run in the order S(g), O(g-1), S(g+1), O(g), ...: the scores of the
-// next block overlap the softmax of this one, and the loads run ahead of both.
-// S^T is double-buffered in TMEM (2 x 64 columns) and O^T takes 4 x 64.  The
+// A block's latent rows are gathered once into four slots of 128 latent
+// columns (slot p always holds columns 128p..128p+127 of the current block);
+// the block's output MMAs free the slots in order and the next block's rows
+// refill them while the remaining output MMAs run.  (Gathering every row twice,
+// into separate score and output rings so that the next block's scores could
+// overlap this block's softmax, measured slower: the gather rate, not the
+// MMAs, bounds this kernel.)  S^T is double-buffered in TMEM (2 x 64 columns)
+// and O^T takes 4 x 64.  The
 // online softmax keeps one reference maximum m per head and rescales O^T in
 // TMEM only when a block's score exceeds m by more than 8 in the base-2
 // exponent; P = 2^(s*scale*log2(e) - m) <= 256 goes to shared memory in BF16.
@@ -56,20 +59,18 @@ constexpr int kThreads = 512;
 constexpr int kSmThreads = 128;         // warps 4..7
 constexpr int kLoaders = 256;           // warps 8..15
 constexpr int kLoaderWarps = kLoaders / 32;
-constexpr int kKPieces = kBT * 8 / kLoaders;    // 16-byte pieces per loader and score chunk
-constexpr int kVPieces = kBT * 16 / kLoaders;   // ... and per value pair
+constexpr int kVPieces = kBT * 16 / kLoaders;   // 16-byte pieces per loader and slot
 // register split (setmaxnreg): 512 threads x 128 at launch; the control / MMA
-// and loader warpgroups give up most of theirs to the softmax warpgroup
+// and loader warpgroups give up part of theirs to the softmax warpgroup
 // (16 loader warps measured no faster than 8: the gather is bound by the
 // memory path, not by issue)
-constexpr int kRegsSoftmax = 232, kRegsOther = 56;
+constexpr int kRegsSoftmax = 232, kRegsOther = 80;
 static_assert(128 * kRegsOther + 128 * kRegsSoftmax + kLoaders * kRegsOther <=
                   (65536 / kThreads) / 8 * 8 * kThreads,
               "register split above the launch's register budget");
 constexpr int kChunk = kBT * 128;       // 64 latent columns of a block: 16 KiB
 constexpr int kPair = 2 * kChunk;       // 128 latent columns of a block: 32 KiB
-constexpr int kKSlots = 4;              // score-side ring (chunks)
-constexpr int kVSlots = 2;              // value-side ring (pairs)
+constexpr int kCSlots = 4;              // 128-column slots of one block
 constexpr int kInfoSlots = 4;
 constexpr int kOParts = kDc / 128;      // O^T in 128-row (latent) parts of 64 columns
 constexpr int kQChunk = kH * 128;       // 64 latent columns of the query block: 8 KiB
@@ -80,9 +81,8 @@ constexpr int kTmemCols = 512;          // S^T: 0..127, O^T: 128..383
 
 // shared memory (from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + 8 * kQChunk;           // 65536
-constexpr int kOffV = kOffK + kKSlots * kChunk;      // 131072
-constexpr int kOffP = kOffV + kVSlots * kPair;       // 196608
+constexpr int kOffC = kOffQ + 8 * kQChunk;           // 65536
+constexpr int kOffP = kOffC + kCSlots * kPair;       // 196608
 constexpr int kOffRed = kOffP + 2 * kQChunk;         // 212992: [4][64] floats
 constexpr int kOffM = kOffRed + 4 * kH * 4;          // reference maxima [64]
 constexpr int kOffL = kOffM + kH * 4;                // per-head scratch [64]
@@ -91,8 +91,8 @@ constexpr int kOffInfo = kOffFlag + 32;              // BInfo [kInfoSlots]
 constexpr int kOffTok = kOffInfo + kInfoSlots * 32;   // token ids [kInfoSlots][128]
 constexpr int kOffBar = kOffTok + kInfoSlots * kBT * 4;
 enum {
-    BQ_FULL = 0, BQ_EMPTY, BK_FULL, BK_EMPTY = BK_FULL + kKSlots, BV_FULL = BK_EMPTY + kKSlots,
-    BV_EMPTY = BV_FULL + kVSlots, BS_FULL = BV_EMPTY + kVSlots, BS_EMPTY = BS_FULL + 2,
+    BQ_FULL = 0, BQ_EMPTY, BC_FULL, BC_EMPTY = BC_FULL + kCSlots, BS_FULL = BC_EMPTY + kCSlots,
+    BS_EMPTY = BS_FULL + 2,
     BP_FULL = BS_EMPTY + 2, BP_EMPTY, BO_FULL, BO_EMPTY, BI_FULL,
     BI_EMPTY = BI_FULL + kInfoSlots, BDRAIN = BI_EMPTY + kInfoSlots, NBARS
 };
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = ptx::smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ, sK = sbase + kOffK, sV = sbase + kOffV, sP = sbase + kOffP;
+    const uint32_t sQ = sbase + kOffQ, sC = sbase + kOffC, sP = sbase + kOffP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     auto bar = [&](int i) { return ptx::smem_u32(&bars[i]); };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kOffMisc);
@@ -257,13 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(BQ_FULL), 1);
         ptx::mbar_init(bar(BQ_EMPTY), 1);
-        for (int i = 0; i < kKSlots; ++i) {
-            ptx::mbar_init(bar(BK_FULL + i), kLoaders);
-            ptx::mbar_init(bar(BK_EMPTY + i), 1);
-        }
-        for (int i = 0; i < kVSlots; ++i) {
-            ptx::mbar_init(bar(BV_FULL + i), kLoaders);
-            ptx::mbar_init(bar(BV_EMPTY + i), 1);
+        for (int i = 0; i < kCSlots; ++i) {
+            ptx::mbar_init(bar(BC_FULL + i), kLoaders);
+            ptx::mbar_init(bar(BC_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar(BS_FULL + i), 1);
@@ -351,44 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::make_idesc(1u, kBT, kH);
             constexpr uint32_t idesc_pv = idesc_qk | ptx::kIdescAMajorMN;
-            int g = 0, kslot = 0, vslot = 0;
-            uint32_t kph = 0, vph = 0, q_ph = 0, p_ph = 0, o_ph = 0;
-            bool any = false, have_prev = false;
-            BInfo prev{};
-            // O^T += C_blk^T . P^T for block x (its P is complete)
-            auto values = [&](const BInfo &x) {
-                if (!wait_bar(bar(BP_FULL), p_ph, sy)) return false;
-                p_ph ^= 1;
-                if (x.b == 0 && !wait_bar(bar(BO_EMPTY), o_ph ^ 1, sy)) return false;
-                ptx::tc_fence_after();
-                for (int pr = 0; pr < 4; ++pr) {
-                    if (!wait_bar(bar(BV_FULL + vslot), vph, sy)) return false;
-                    ptx::tc_fence_after();
-                    const uint32_t a0 = sV + vslot * kPair;
-                    for (int kk = 0; kk < x.ksteps; ++kk) {
-                        const uint64_t ad = ptx::smem_desc_mn_sw128(a0 + kk * 2048, kChunk);
-                        const uint64_t bd = ptx::smem_desc_sw128(sP + (kk >> 2) * kQChunk) + (kk & 3) * 2;
-                        ptx::mma_bf16(tmem + 128 + pr * kH, ad, bd, idesc_pv, (x.b > 0 || kk > 0));
-                    }
-                    ptx::mma_commit(bar(BV_EMPTY + vslot));
-                    if (++vslot == kVSlots) { vslot = 0; vph ^= 1; }
-                }
-                ptx::mma_commit(bar(BP_EMPTY));
-                if (x.b == x.nb - 1) {
-                    ptx::mma_commit(bar(BO_FULL));
-                    o_ph ^= 1;
-                }
-                return true;
-            };
+            int g = 0;
+            uint32_t c_ph = 0, q_ph = 0, p_ph = 0, o_ph = 0;
+            bool any = false;
             for (;;) {
                 const int is = g % kInfoSlots;
                 if (!wait_bar(bar(BI_FULL + is), (g / kInfoSlots) & 1, sy)) break;
                 const BInfo in = info[is];
                 ptx::mbar_arrive(bar(BI_EMPTY + is));
-                if (in.t < 0) {
-                    if (have_prev) values(prev);
-                    break;
-                }
+                if (in.t < 0) break;
                 if (in.b == 0) {
                     if (!wait_bar(bar(BQ_FULL), q_ph, sy)) break;
                     q_ph ^= 1;
@@ -398,27 +365,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 bool ok = true;
                 // S^T = C_blk . Q^T over the 512 latent columns
-                for (int c = 0; c < 8; ++c) {
-                    if (!wait_bar(bar(BK_FULL + kslot), kph, sy)) {
+                for (int sl = 0; sl < kCSlots; ++sl) {
+                    if (!wait_bar(bar(BC_FULL + sl), c_ph, sy)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint64_t ad = ptx::smem_desc_sw128(sK + kslot * kChunk);
-                    const uint64_t bd = ptx::smem_desc_sw128(sQ + c * kQChunk);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_bf16(tmem + sb * kH, ad + kk * 2, bd + kk * 2, idesc_qk, (c | kk) != 0);
-                    ptx::mma_commit(bar(BK_EMPTY + kslot));
-                    if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t ad = ptx::smem_desc_sw128(sC + sl * kPair + h * kChunk);
+                        const uint64_t bd = ptx::smem_desc_sw128(sQ + (2 * sl + h) * kQChunk);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            ptx::mma_bf16(tmem + sb * kH, ad + kk * 2, bd + kk * 2, idesc_qk,
+                                          (sl | h | kk) != 0);
+                    }
                     any = true;
                 }
                 if (!ok) break;
                 ptx::mma_commit(bar(BS_FULL + sb));
                 if (in.b == in.nb - 1) ptx::mma_commit(bar(BQ_EMPTY));
-                if (have_prev && !values(prev)) break;
-                prev = in;
-                have_prev = true;
+                // O^T += C_blk^T . P^T once P is complete; each slot is freed as
+                // soon as its MMAs are done
+                if (!wait_bar(bar(BP_FULL), p_ph, sy)) break;
+                p_ph ^= 1;
+                if (in.b == 0 && !wait_bar(bar(BO_EMPTY), o_ph ^ 1, sy)) break;
+                ptx::tc_fence_after();
+                for (int sl = 0; sl < kCSlots; ++sl) {
+                    const uint32_t a0 = sC + sl * kPair;
+                    for (int kk = 0; kk < in.ksteps; ++kk) {
+                        const uint64_t ad = ptx::smem_desc_mn_sw128(a0 + kk * 2048, kChunk);
+                        const uint64_t bd = ptx::smem_desc_sw128(sP + (kk >> 2) * kQChunk) + (kk & 3) * 2;
+                        ptx::mma_bf16(tmem + 128 + sl * kH, ad, bd, idesc_pv, (in.b > 0 || kk > 0));
+                    }
+                    ptx::mma_commit(bar(BC_EMPTY + sl));
+                }
+                ptx::mma_commit(bar(BP_EMPTY));
+                if (in.b == in.nb - 1) {
+                    ptx::mma_commit(bar(BO_FULL));
+                    o_ph ^= 1;
+                }
+                c_ph ^= 1;
                 ++g;
             }
             if (any) {
@@ -691,14 +678,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             return wait_bar(b, parity, sy);
         };
         bool ok = true;
-        int g = 0, kslot = 0, vslot = 0, prev_is = 0;
-        uint32_t kph = 0, vph = 0;
-        bool have_prev = false;
-        // the 4 column pairs (128 latent columns each) of block slot `ts`: this
-        // thread copies 16-byte piece lt % 16 of rows lt / 16 + (kLoaders / 16) s;
-        // the rows' source and destination are set up once per block
-        auto load_values = [&](int ts) {
-            const int *tk = toks + ts * kBT;
+        int g = 0;
+        uint32_t c_ph = 0;
+        for (;;) {
+            const int is = g % kInfoSlots;
+            ok = ok && acquire(bar(BI_FULL + is), (g / kInfoSlots) & 1);
+            if (!ok || info[is].t < 0) break;
+            // this thread copies 16-byte piece lt % 16 of rows lt / 16 + (kLoaders / 16) s
+            // of each slot; the rows' source and destination are set up once
+            const int *tk = toks + is * kBT;
             const int k = lt & 15;
             const char *src[kVPieces];
             uint32_t off[kVPieces], sz = 0;
@@ -710,64 +698,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 off[s8] = (k >> 3) * kChunk + r * 128 + (((k & 7) ^ (r & 7)) << 4);
                 sz |= (tok >= 0 ? 1u : 0u) << s8;
             }
-            for (int pr = 0; pr < 4 && ok; ++pr) {
-                ok = acquire(bar(BV_EMPTY + vslot), vph ^ 1);
+            __syncwarp();
+            if ((lt & 31) == 0) ptx::mbar_arrive(bar(BI_EMPTY + is));   // token ids read
+            for (int sl = 0; sl < kCSlots && ok; ++sl) {
+                ok = acquire(bar(BC_EMPTY + sl), c_ph ^ 1);
                 if (!ok) break;
-                const uint32_t dst0 = sV + vslot * kPair;
+                const uint32_t dst0 = sC + sl * kPair;
 #pragma unroll
                 for (int s8 = 0; s8 < kVPieces; ++s8)
-                    ptx::cp_async16(dst0 + off[s8], src[s8] + ((sz >> s8) & 1u) * (pr * 256),
+                    ptx::cp_async16(dst0 + off[s8], src[s8] + ((sz >> s8) & 1u) * (sl * 256),
                                     ((sz >> s8) & 1u) * 16u);
                 ptx::cp_async_commit();
-                push(bar(BV_FULL + vslot));
-                if (++vslot == kVSlots) { vslot = 0; vph ^= 1; }
+                push(bar(BC_FULL + sl));
             }
-        };
-        for (;;) {
-            const int is = g % kInfoSlots;
-            ok = ok && acquire(bar(BI_FULL + is), (g / kInfoSlots) & 1);
-            if (!ok) break;
-            const int t_in = info[is].t;
-            if (t_in < 0) {
-                if (have_prev) load_values(prev_is);
-                break;
-            }
-            // this block's score-side chunks (64 latent columns each): piece lt % 8
-            // of rows lt / 8 + (kLoaders / 8) s
-            {
-                const int *tk = toks + is * kBT;
-                const int k = lt & 7;
-                const char *src[kKPieces];
-                uint32_t off[kKPieces], sz = 0;
-#pragma unroll
-                for (int s4 = 0; s4 < kKPieces; ++s4) {
-                    const int r = (lt >> 3) + (kLoaders / 8) * s4;
-                    const int tok = tk[r];
-                    src[s4] = kvb + (tok >= 0 ? static_cast<int64_t>(tok) * (kDc * 2) + k * 16 : 0);
-                    off[s4] = r * 128 + ((k ^ (r & 7)) << 4);
-                    sz |= (tok >= 0 ? 1u : 0u) << s4;
-                }
-                for (int c = 0; c < 8 && ok; ++c) {
-                    ok = acquire(bar(BK_EMPTY + kslot), kph ^ 1);
-                    if (!ok) break;
-                    const uint32_t dst0 = sK + kslot * kChunk;
-#pragma unroll
-                    for (int s4 = 0; s4 < kKPieces; ++s4)
-                        ptx::cp_async16(dst0 + off[s4], src[s4] + ((sz >> s4) & 1u) * (c * 128),
-                                        ((sz >> s4) & 1u) * 16u);
-                    ptx::cp_async_commit();
-                    push(bar(BK_FULL + kslot));
-                    if (++kslot == kKSlots) { kslot = 0; kph ^= 1; }
-                }
-            }
-            // the previous block's value-side pairs, then its record is free
-            if (ok && have_prev) {
-                load_values(prev_is);
-                __syncwarp();
-                if ((lt & 31) == 0) ptx::mbar_arrive(bar(BI_EMPTY + prev_is));
-            }
-            prev_is = is;
-            have_prev = true;
+            c_ph ^= 1;
             ++g;
         }
         flush();
