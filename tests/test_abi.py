@@ -127,6 +127,23 @@ def test_host_validation_rejects_bad_arguments(lib):
         # kpool_expand_indices: index_topk not a multiple of kpool; n_docs without cu_seqlens
         (L.kpool_expand_indices, (p, None, None, 1, 1024, 4, 2046, 1, p, None), -1),
         (L.kpool_expand_indices, (p, None, None, 2, 1024, 4, 2048, 1, p, None), -1),
+        # kpool_sparse_mla_fwd: heads / latent width outside the built shape, scale <= 0,
+        # misaligned q, short workspace, negative width, no token list
+        (L.kpool_sparse_mla_fwd, (p, p, p, 16, 16, 4, 32, 512, 0.1, p, p, p, 256, None), -2),
+        (L.kpool_sparse_mla_fwd, (p, p, p, 16, 16, 4, 64, 256, 0.1, p, p, p, 256, None), -2),
+        (L.kpool_sparse_mla_fwd, (p, p, p, 16, 16, 4, 64, 512, 0.0, p, p, p, 256, None), -1),
+        (L.kpool_sparse_mla_fwd, (p_mis, p, p, 16, 16, 4, 64, 512, 0.1, p, p, p, 256, None), -1),
+        (L.kpool_sparse_mla_fwd, (p, p, p, 16, 16, 4, 64, 512, 0.1, p, p, p, 16, None), -4),
+        (L.kpool_sparse_mla_fwd, (p, p, p, 16, 16, -1, 64, 512, 0.1, p, p, p, 256, None), -1),
+        (L.kpool_sparse_mla_fwd, (p, p, None, 16, 16, 4, 64, 512, 0.1, p, p, p, 256, None), -1),
+        # kpool_sparse_mla_fwd_pools: index_topk not a multiple of kpool, n_docs without
+        # cu_seqlens; _pools_at: missing per-document arrays
+        (L.kpool_sparse_mla_fwd_pools, (p, p, p, None, None, 1, 16, 64, 512, 4, 2046, 1, 0.1,
+                                        p, p, p, 256, None), -1),
+        (L.kpool_sparse_mla_fwd_pools, (p, p, p, None, None, 2, 16, 64, 512, 4, 2048, 1, 0.1,
+                                        p, p, p, 256, None), -1),
+        (L.kpool_sparse_mla_fwd_pools_at, (p, p, p, None, p, p, p, 1, 16, 16, 64, 512, 4, 2048, 1,
+                                           0.1, p, p, p, 256, None), -1),
     ]
     for fn, args, code in cases:
         rc = fn(*args)

@@ -156,17 +156,23 @@ def _synth_pools(rng, cu, kp, Kp, q_rows=None):
 
 
 @pytest.mark.parametrize("kp,tail,docs", [(4, True, None), (4, False, None), (3, True, None),
-                                          (4, True, (5, (100, 450)))])
+                                          (1, True, None), (8, True, None),
+                                          (4, True, (5, (100, 450), None)),
+                                          (8, False, (4, (100, 900), 1))])
 def test_fused_expansion(K, ora, kp, tail, docs):
     """kpool_sparse_mla_fwd_pools equals kpool_sparse_mla_fwd on the tokens
     kpool_expand_indices writes (bit for bit), and the oracle on the oracle's
-    expansion."""
+    expansion: kpool 1, 3, 4, 8, with and without the tail, one sequence or
+    packed documents (one of them empty)."""
     dev = torch.device("cuda")
     T, index_topk = 2500, 96 * kp
     Kp = index_topk // kp
     if docs:
         lens = np.random.default_rng(docs[0]).integers(docs[1][0], docs[1][1], size=docs[0])
+        if docs[2] is not None:
+            lens[docs[2]] = 0                     # an empty document
         lens[-1] += T - lens.sum()
+        assert lens.min() >= 0
         cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     else:
         cu = np.array([0, T], np.int32)
