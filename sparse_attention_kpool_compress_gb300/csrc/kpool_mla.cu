@@ -37,10 +37,10 @@
 // into separate score and output rings so that the next block's scores could
 // overlap this block's softmax, measured slower: the gather rate, not the
 // MMAs, bounds this kernel.)  S^T is double-buffered in TMEM (2 x 64 columns)
-// and O^T takes 4 x 64.  The
-// online softmax keeps one reference maximum m per head and rescales O^T in
-// TMEM only when a block's score exceeds m by more than 8 in the base-2
-// exponent; P = 2^(s*scale*log2(e) - m) <= 256 goes to shared memory in BF16.
+// and O^T takes 4 x 64.  The online softmax keeps one reference maximum m per
+// head and rescales O^T in TMEM only when a block's score exceeds m by more
+// than 8 in the base-2 exponent; P = 2^(s*scale*log2(e) - m) <= 256 goes to
+// shared memory in BF16.
 #include <cuda_bf16.h>
 
 #include <algorithm>
