@@ -59,7 +59,6 @@ constexpr int kThreads = 512;
 constexpr int kSmThreads = 128;         // warps 4..7
 constexpr int kLoaders = 256;           // warps 8..15
 constexpr int kLoaderWarps = kLoaders / 32;
-constexpr int kVPieces = kBT * 16 / kLoaders;   // 16-byte pieces per loader and slot
 // register split (setmaxnreg): 512 threads x 128 at launch; the control / MMA
 // and loader warpgroups give up part of theirs to the softmax warpgroup
 // (16 loader warps measured no faster than 8: the gather is bound by the
@@ -71,6 +70,7 @@ static_assert(128 * kRegsOther + 128 * kRegsSoftmax + kLoaders * kRegsOther <=
 constexpr int kChunk = kBT * 128;       // 64 latent columns of a block: 16 KiB
 constexpr int kPair = 2 * kChunk;       // 128 latent columns of a block: 32 KiB
 constexpr int kCSlots = 4;              // 128-column slots of one block
+static_assert(kLoaders == 64 * kCSlots, "two loader warps per slot");
 constexpr int kInfoSlots = 4;
 constexpr int kOParts = kDc / 128;      // O^T in 128-row (latent) parts of 64 columns
 constexpr int kQChunk = kH * 128;       // 64 latent columns of the query block: 8 KiB
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(BQ_FULL), 1);
         ptx::mbar_init(bar(BQ_EMPTY), 1);
         for (int i = 0; i < kCSlots; ++i) {
-            ptx::mbar_init(bar(BC_FULL + i), kLoaders);
+            ptx::mbar_init(bar(BC_FULL + i), 64);   // the slot's two loader warps
             ptx::mbar_init(bar(BC_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -642,79 +642,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         ptx::setmaxnreg_dec<kRegsOther>();
         // ---------------- loaders ----------------
-        const int lt = threadIdx.x - 256;   // 0..kLoaders-1
-        const char *kvb = reinterpret_cast<const char *>(p.kv);
-        // barriers of committed cp.async groups not yet signalled (oldest first)
-        uint32_t pend0 = 0, pend1 = 0, pend2 = 0;
-        int npend = 0;
-        auto push = [&](uint32_t b) {
-            if (npend == 0) pend0 = b;
-            else if (npend == 1) pend1 = b;
-            else pend2 = b;
-            ++npend;
-            if (npend > 2) {   // keep two groups in flight
-                ptx::cp_async_wait_group<2>();
-                ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(pend0);
-                pend0 = pend1;
-                pend1 = pend2;
-                --npend;
-            }
-        };
-        auto flush = [&]() {
-            if (npend == 0) return;
-            ptx::cp_async_wait_all();
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(pend0);
-            if (npend > 1) ptx::mbar_arrive(pend1);
-            if (npend > 2) ptx::mbar_arrive(pend2);
-            npend = 0;
-        };
-        // completed copies are signalled before blocking: the consumer may
-        // need them to make progress
-        auto acquire = [&](uint32_t b, uint32_t parity) {
-            if (ptx::mbar_try_wait(b, parity)) return true;
-            flush();
-            return wait_bar(b, parity, sy);
-        };
+        // Each slot has its own pair of warps, so the four slots of a block
+        // refill independently as the output MMAs free them: a pair waits only
+        // for its own copies (then a proxy fence and its arrival on the slot).
+        const int sl = (warp - 8) >> 1;                   // the slot of this pair
+        const int t64 = ((warp - 8) & 1) * 32 + lane;     // 0..63 within the pair
+        const int k = t64 & 15;                           // 16-byte piece of the slot's 256 bytes
+        const char *kvb = reinterpret_cast<const char *>(p.kv) + sl * 256 + k * 16;
+        const uint32_t dst_slot = sC + sl * kPair + (k >> 3) * kChunk;
         bool ok = true;
         int g = 0;
         uint32_t c_ph = 0;
         for (;;) {
             const int is = g % kInfoSlots;
-            ok = ok && acquire(bar(BI_FULL + is), (g / kInfoSlots) & 1);
+            ok = ok && wait_bar_warp(bar(BI_FULL + is), (g / kInfoSlots) & 1, sy);
             if (!ok || info[is].t < 0) break;
-            // this thread copies 16-byte piece lt % 16 of rows lt / 16 + (kLoaders / 16) s
-            // of each slot; the rows' source and destination are set up once
+            ok = wait_bar_warp(bar(BC_EMPTY + sl), c_ph ^ 1, sy);
+            if (!ok) break;
             const int *tk = toks + is * kBT;
-            const int k = lt & 15;
-            const char *src[kVPieces];
-            uint32_t off[kVPieces], sz = 0;
-#pragma unroll
-            for (int s8 = 0; s8 < kVPieces; ++s8) {
-                const int r = (lt >> 4) + (kLoaders / 16) * s8;
+#pragma unroll 8
+            for (int i = 0; i < kBT / 4; ++i) {           // rows t64 / 16 + 4 i
+                const int r = (t64 >> 4) + 4 * i;
                 const int tok = tk[r];
-                src[s8] = kvb + (tok >= 0 ? static_cast<int64_t>(tok) * (kDc * 2) + k * 16 : 0);
-                off[s8] = (k >> 3) * kChunk + r * 128 + (((k & 7) ^ (r & 7)) << 4);
-                sz |= (tok >= 0 ? 1u : 0u) << s8;
+                ptx::cp_async16(dst_slot + r * 128 + (((k & 7) ^ (r & 7)) << 4),
+                                kvb + (tok >= 0 ? static_cast<int64_t>(tok) * (kDc * 2) : 0),
+                                tok >= 0 ? 16u : 0u);
             }
             __syncwarp();
-            if ((lt & 31) == 0) ptx::mbar_arrive(bar(BI_EMPTY + is));   // token ids read
-            for (int sl = 0; sl < kCSlots && ok; ++sl) {
-                ok = acquire(bar(BC_EMPTY + sl), c_ph ^ 1);
-                if (!ok) break;
-                const uint32_t dst0 = sC + sl * kPair;
-#pragma unroll
-                for (int s8 = 0; s8 < kVPieces; ++s8)
-                    ptx::cp_async16(dst0 + off[s8], src[s8] + ((sz >> s8) & 1u) * (sl * 256),
-                                    ((sz >> s8) & 1u) * 16u);
-                ptx::cp_async_commit();
-                push(bar(BC_FULL + sl));
-            }
+            if (lane == 0) ptx::mbar_arrive(bar(BI_EMPTY + is));   // token ids read
+            ptx::cp_async_commit();
+            ptx::cp_async_wait_all();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bar(BC_FULL + sl));
             c_ph ^= 1;
             ++g;
         }
-        flush();
         ptx::cp_async_wait_all();
     }
 
