@@ -29,7 +29,7 @@
 // Both contractions run transposed, so every MMA has M = 128 and the 64
 // heads are its N dimension:
 //   S^T [128 tokens x 64 heads]   = C_blk [128 x 512] . Q^T          (A, B K-major)
-//   O^T [512 latent x 64 heads]  += C_blk^T [512 x 128] . P^T        (A MN-major)
+//   O^T [512 latent x 64 heads]  += C_blk^T [512 x 128] . P          (A, B MN-major)
 // A block's latent rows are gathered once into four slots of 128 latent
 // columns (slot p always holds columns 128p..128p+127 of the current block);
 // the block's output MMAs free the slots in order and the next block's rows
@@ -40,7 +40,9 @@
 // and O^T takes 4 x 64.  The online softmax keeps one reference maximum m per
 // head and rescales O^T in TMEM only when a block's score exceeds m by more
 // than 8 in the base-2 exponent; P = 2^(s*scale*log2(e) - m) <= 256 goes to
-// shared memory in BF16.
+// shared memory in BF16, one 128-byte row of 64 heads per listed token.  Each
+// softmax thread exponentiates its row against the current maxima before the
+// warps agree on whether a rescale is due, so the common block needs one pass.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::make_idesc(1u, kBT, kH);
-            constexpr uint32_t idesc_pv = idesc_qk | ptx::kIdescAMajorMN;
+            constexpr uint32_t idesc_pv = idesc_qk | ptx::kIdescAMajorMN | ptx::kIdescBMajorMN;
             int g = 0;
             uint32_t c_ph = 0, q_ph = 0, p_ph = 0, o_ph = 0;
             bool any = false;
@@ -395,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a0 = sC + sl * kPair;
                     for (int kk = 0; kk < in.ksteps; ++kk) {
                         const uint64_t ad = ptx::smem_desc_mn_sw128(a0 + kk * 2048, kChunk);
-                        const uint64_t bd = ptx::smem_desc_sw128(sP + (kk >> 2) * kQChunk) + (kk & 3) * 2;
+                        const uint64_t bd = ptx::smem_desc_mn_sw128(sP + kk * 2048, 2 * kQChunk);
                         ptx::mma_bf16(tmem + 128 + sl * kH, ad, bd, idesc_pv, (in.b > 0 || kk > 0));
                     }
                     ptx::mma_commit(bar(BC_EMPTY + sl));
@@ -426,7 +428,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *red = reinterpret_cast<float *>(smem + kOffRed);
         float *hs = reinterpret_cast<float *>(smem + kOffL);
         volatile uint32_t *flags = reinterpret_cast<volatile uint32_t *>(smem + kOffFlag);
-        uint8_t *Pb = smem + kOffP;
         const float c = p.c_scale;
         float l[kH];                               // this thread's partial sums per head
         int blk = 0, agr = 0;
@@ -456,17 +457,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        // the reference maxima (shared, read as broadcasts)
-        auto load_m = [&](float (&mr)[kH]) {
+        // v = 2^(v * c - m) in place against the reference maxima (shared, read
+        // as broadcasts), 0 for a token that is not listed; true when some
+        // exponent exceeds the rescale headroom
+        auto exponentiate = [&](float (&v)[kH], bool valid_row) {
+            bool over = false;
             const float4 *m4 = reinterpret_cast<const float4 *>(m_s);
 #pragma unroll
             for (int i = 0; i < kH / 4; ++i) {
                 const float4 x = m4[i];
-                mr[4 * i] = x.x;
-                mr[4 * i + 1] = x.y;
-                mr[4 * i + 2] = x.z;
-                mr[4 * i + 3] = x.w;
+                const float mq[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = fmaf(v[4 * i + e], c, -mq[e]);
+                    over |= a > kRescale;
+                    v[4 * i + e] = valid_row ? ptx::ex2_approx(a) : 0.f;
+                }
             }
+            return over;
         };
         auto load_s = [&](int bs, float (&v)[kH]) {
             uint32_t a[32], b2[32];
@@ -480,6 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         bool bad = false;   // a wait of the previous round failed in this warp
+        // this thread's row of P (64 heads, BF16) in a 128-byte-swizzled tile
+        const uint32_t prow = sP + r * 128;
         for (;;) {
             const int bs = blk & 1;
             const uint32_t bph = (blk >> 1) & 1;
@@ -493,6 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool end = ok && in.t < 0;
             const bool valid = ok && !end && ((in.mask[sub] >> lane) & 1u);
             bool need = false;
+            // the block's probabilities, taken against the current reference
+            // maxima before the warps agree (kept unless a rescale is needed);
+            // defined on every path, so that none stays live across rounds
+            float pv[kH];
+#pragma unroll
+            for (int h = 0; h < kH; ++h) pv[h] = 0.f;
             if (ok && !end) {
                 ok = wait_bar_warp(bar(BS_FULL + bs), bph, sy);
                 if (ok) {
@@ -502,12 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int h = 0; h < kH; ++h) l[h] = 0.f;
                     } else {
-                        float v[kH], mr[kH];
-                        load_s(bs, v);
-                        load_m(mr);
-#pragma unroll
-                        for (int h = 0; h < kH; ++h) need |= fmaf(v[h], c, -mr[h]) > kRescale;
-                        need = need && valid;
+                        load_s(bs, pv);
+                        need = exponentiate(pv, valid) && valid;
                     }
                 }
             }
@@ -516,13 +528,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (all & 3u) break;
             if (all & 4u) {
                 // exact block maximum per head, new reference maxima, rescale
-                float v[kH];
-                load_s(bs, v);
+                load_s(bs, pv);
 #pragma unroll
-                for (int h = 0; h < kH; ++h) v[h] = valid ? v[h] * c : -INFINITY;
-                warp_reduce(v, true);
-                red[sub * kH + 2 * lane] = v[0];
-                red[sub * kH + 2 * lane + 1] = v[1];
+                for (int h = 0; h < kH; ++h) pv[h] = valid ? pv[h] * c : -INFINITY;
+                warp_reduce(pv, true);
+                red[sub * kH + 2 * lane] = pv[0];
+                red[sub * kH + 2 * lane + 1] = pv[1];
                 ptx::named_bar_sync(3, kSmThreads);
                 if (sub == 0) {
 #pragma unroll
@@ -550,7 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (scale_o) {
                         // every PV MMA of the earlier blocks has completed (their
-                        // completion precedes this block's scores)
+                        // completion precedes this block's scores); the factors
+                        // are re-read per part rather than held in registers
+                        const volatile float *hsv = hs;
 #pragma unroll 1
                         for (int sl = 0; sl < kOParts; ++sl) {
 #pragma unroll
@@ -561,32 +574,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ptx::tmem_ld_wait(ov);
 #pragma unroll
                                 for (int i = 0; i < 32; ++i)
-                                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * hs[half * 32 + i]);
+                                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * hsv[half * 32 + i]);
                                 ptx::tmem_st32(ta, ov);
                             }
                         }
                         ptx::tmem_st_wait();
                     }
                 }
+                // (unconditional, so that no earlier value of pv stays live
+                // across the rescale)
+                load_s(bs, pv);
+                exponentiate(pv, valid);
             } else {
                 bad = !wait_bar_warp(bar(BP_EMPTY), (blk & 1) ^ 1, sy);
             }
-            // probabilities: P^T[h][r] (BF16) and the partial sums
+            // P[r][h] (BF16, eight heads per 16-byte piece) and the partial sums
             if (!bad) {
-                float v[kH], mr[kH];
-                load_s(bs, v);
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(BS_EMPTY + bs));
-                load_m(mr);
-                uint8_t *pr = Pb + (r >> 6) * kQChunk + (r & 7) * 2;
-                const int piece = (r & 63) >> 3;
 #pragma unroll
-                for (int h = 0; h < kH; ++h) {
-                    const float pv = valid ? ptx::ex2_approx(fmaf(v[h], c, -mr[h])) : 0.f;
-                    l[h] += pv;
-                    *reinterpret_cast<__nv_bfloat16 *>(pr + h * 128 + ((piece ^ (h & 7)) << 4)) =
-                        __float2bfloat16_rn(pv);
+                for (int j = 0; j < kH / 8; ++j) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int h = 8 * j + 2 * i;
+                        l[h] += pv[h];
+                        l[h + 1] += pv[h + 1];
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(pv[h], pv[h + 1]);
+                        w[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    ptx::st_shared_v4(prow + ((j ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();

@@ -304,8 +304,18 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t 
     return d;
 }
 
-// Instruction-descriptor bit: operand A is MN-major (transposed).
+// Instruction-descriptor bits: operand A (B) is MN-major (transposed).
 constexpr uint32_t kIdescAMajorMN = 1u << 15;
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
+
+// 16-byte shared-memory store.
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
 
 // ---- cp.async (16 bytes, L2 only) ------------------------------------------
 // src_bytes = 0 reads nothing and fills the 16 destination bytes with zeros.
