@@ -164,6 +164,11 @@ struct Params {
     Layout L;
 };
 
+// 2 relu(x), exactly (x + |x| is 2x or +0), as one add with an absolute-value
+// operand on the FMA pipe rather than a max on the ALU pipe; the head weights are
+// staged halved to match.
+__device__ __forceinline__ float twice_relu(float x) { return __fadd_rn(x, fabsf(x)); }
+
 // Orderable key of a score: larger float -> larger key; -0 folded into +0.
 __device__ __forceinline__ uint32_t fkey(float f)
 {
@@ -1032,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v = __ldg(p.w + off);
                     if (p.fp8) v *= __ldg(p.q_scale + off);
                 }
-                wsm[etid] = v;
+                wsm[etid] = 0.5f * v;   // halved: the head sums take 2 relu(x) = x + |x|
             }
             ptx::named_bar_sync(1, kEpiThreads);
             if (*agree_ti != 0u || t.t0 < 0) break;   // the same outcome in every warp
@@ -1083,17 +1088,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int qj = kHalfQ ? 0 : (8 * j) / H;
-                    a[qj][0] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(va[4 * j]), 0.f),
-                                                          fmaxf(__uint_as_float(va[4 * j + 1]), 0.f)),
+                    a[qj][0] = ptx::ffma2(ptx::pack_f32x2(twice_relu(__uint_as_float(va[4 * j])),
+                                                          twice_relu(__uint_as_float(va[4 * j + 1]))),
                                           wq[j], a[qj][0]);
-                    a[qj][1] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(va[4 * j + 2]), 0.f),
-                                                          fmaxf(__uint_as_float(va[4 * j + 3]), 0.f)),
+                    a[qj][1] = ptx::ffma2(ptx::pack_f32x2(twice_relu(__uint_as_float(va[4 * j + 2])),
+                                                          twice_relu(__uint_as_float(va[4 * j + 3]))),
                                           wq[j], a[qj][1]);
-                    a[qj][2] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(vb[4 * j]), 0.f),
-                                                          fmaxf(__uint_as_float(vb[4 * j + 1]), 0.f)),
+                    a[qj][2] = ptx::ffma2(ptx::pack_f32x2(twice_relu(__uint_as_float(vb[4 * j])),
+                                                          twice_relu(__uint_as_float(vb[4 * j + 1]))),
                                           wq[j], a[qj][2]);
-                    a[qj][3] = ptx::ffma2(ptx::pack_f32x2(fmaxf(__uint_as_float(vb[4 * j + 2]), 0.f),
-                                                          fmaxf(__uint_as_float(vb[4 * j + 3]), 0.f)),
+                    a[qj][3] = ptx::ffma2(ptx::pack_f32x2(twice_relu(__uint_as_float(vb[4 * j + 2])),
+                                                          twice_relu(__uint_as_float(vb[4 * j + 3]))),
                                           wq[j], a[qj][3]);
                 }
                 const bool b0 = (kq & 1) != 0, b1 = (kq & 2) != 0;
@@ -1140,10 +1145,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int j = kHalfQ ? 0 : col / H;
                         const int k = (col / 4) % NACC;
                         const ulonglong2 wv = w4[col / 4];
-                        const uint64_t r0 = ptx::pack_f32x2(fmaxf(__uint_as_float(v[x]), 0.f),
-                                                            fmaxf(__uint_as_float(v[x + 1]), 0.f));
-                        const uint64_t r1 = ptx::pack_f32x2(fmaxf(__uint_as_float(v[x + 2]), 0.f),
-                                                            fmaxf(__uint_as_float(v[x + 3]), 0.f));
+                        const uint64_t r0 = ptx::pack_f32x2(twice_relu(__uint_as_float(v[x])),
+                                                            twice_relu(__uint_as_float(v[x + 1])));
+                        const uint64_t r1 = ptx::pack_f32x2(twice_relu(__uint_as_float(v[x + 2])),
+                                                            twice_relu(__uint_as_float(v[x + 3])));
                         a4[j][k] = ptx::ffma2(r0, wv.x, a4[j][k]);
                         a4[j][k] = ptx::ffma2(r1, wv.y, a4[j][k]);
                     }
@@ -1187,7 +1192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < QS; ++j) {
                     float v = s[j];
                     if (p.fp8) v *= sk;
-                    s[j] = (v == 0.f) ? 0.f : v;   // fold -0 into +0
+                    s[j] = __fadd_rn(v, 0.f);   // folds -0 into +0
                 }
                 PT_MARK(3);
 
@@ -1289,7 +1294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int pool_local = (t.i0 + tj) * kBM + qr * 32 + own;
                         const int pool_g = t.pool_base + pool_local;
                         if (p.fp8 && pool_g < p.P_total) sv *= p.pk_scale[pool_g];
-                        sv = (sv == 0.f) ? 0.f : sv;   // fold -0 into +0
+                        sv = __fadd_rn(sv, 0.f);   // folds -0 into +0
                         PT_MARK(3);
                         if (owner) {
                             const bool ps = tj < npt && pool_local < nc0 && fkey(sv) > thr0;
