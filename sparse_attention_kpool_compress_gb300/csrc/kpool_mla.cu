@@ -14,15 +14,17 @@
 // the row's selected pools (kpool consecutive tokens each) plus its causal
 // tail, computed on the fly so that the token table never reaches memory.
 //
-// Design (one persistent CTA per SM, 16 warps, rows handed out by an atomic
+// Design (one persistent CTA per SM, 20 warps, rows handed out by an atomic
 // counter):
 //   warp 0      control: the row's 64 x 512 query block (TMA tiled loads) and,
 //               per block of 128 listed tokens, a record (row, block, validity
 //               mask) with the block's token ids in shared memory
 //   warp 1      TMEM allocation and the tcgen05.mma issuer (one thread)
-//   warps 4-7   online softmax and output, one TMEM lane per thread (a
-//               listed token for the scores, a latent column for the output)
-//   warps 8-15  loaders: the listed tokens' latent rows, gathered with 16-byte
+//   warps 4-11  online softmax and output, two warps per TMEM lane quarter
+//               (one TMEM lane per thread: a listed token for the scores, a
+//               latent column for the output; each warp of a pair takes half of
+//               the heads and half of the output parts)
+//   warps 12-19 loaders: the listed tokens' latent rows, gathered with 16-byte
 //               cp.async into 128-byte-swizzled tiles (a gather of 128-byte
 //               rows moves about 3x more bytes per cycle this way than with
 //               one tile::gather4 TMA load per 4 rows)
@@ -57,16 +59,19 @@ namespace {
 constexpr int kH = 64;                  // heads = MMA N
 constexpr int kDc = 512;                // latent width
 constexpr int kBT = 128;                // listed tokens per block = MMA M of S^T
-constexpr int kThreads = 512;
-constexpr int kSmThreads = 128;         // warps 4..7
-constexpr int kLoaders = 256;           // warps 8..15
+constexpr int kThreads = 640;
+constexpr int kSmWarps = 8;             // warps 4..11: two per TMEM lane quarter
+constexpr int kSmThreads = 32 * kSmWarps;
+constexpr int kHh = 32;                 // heads per softmax thread (half of them)
+constexpr int kLoaderWarp0 = 4 + kSmWarps;
+constexpr int kLoaders = 256;           // warps 12..19
 constexpr int kLoaderWarps = kLoaders / 32;
-// register split (setmaxnreg): 512 threads x 128 at launch; the control / MMA
-// and loader warpgroups give up part of theirs to the softmax warpgroup
+// register split (setmaxnreg): 640 threads x 96 at launch; the control / MMA
+// and loader warpgroups give up part of theirs to the two softmax warpgroups
 // (16 loader warps measured no faster than 8: the gather is bound by the
 // memory path, not by issue)
-constexpr int kRegsSoftmax = 232, kRegsOther = 80;
-static_assert(128 * kRegsOther + 128 * kRegsSoftmax + kLoaders * kRegsOther <=
+constexpr int kRegsSoftmax = 136, kRegsOther = 64;
+static_assert(128 * kRegsOther + kSmThreads * kRegsSoftmax + kLoaders * kRegsOther <=
                   (65536 / kThreads) / 8 * 8 * kThreads,
               "register split above the launch's register budget");
 constexpr int kChunk = kBT * 128;       // 64 latent columns of a block: 16 KiB
@@ -88,14 +93,14 @@ constexpr int kOffP = kOffC + kCSlots * kPair;       // 196608
 constexpr int kOffRed = kOffP + 2 * kQChunk;         // 212992: [4][64] floats
 constexpr int kOffM = kOffRed + 4 * kH * 4;          // reference maxima [64]
 constexpr int kOffL = kOffM + kH * 4;                // per-head scratch [64]
-constexpr int kOffFlag = kOffL + kH * 4;             // agreement words [2][4]
-constexpr int kOffInfo = kOffFlag + 32;              // BInfo [kInfoSlots]
+constexpr int kOffFlag = kOffL + kH * 4;             // agreement words [2][kSmWarps]
+constexpr int kOffInfo = kOffFlag + 2 * kSmWarps * 4; // BInfo [kInfoSlots]
 constexpr int kOffTok = kOffInfo + kInfoSlots * 32;   // token ids [kInfoSlots][128]
 constexpr int kOffBar = kOffTok + kInfoSlots * kBT * 4;
 enum {
     BQ_FULL = 0, BQ_EMPTY, BC_FULL, BC_EMPTY = BC_FULL + kCSlots, BS_FULL = BC_EMPTY + kCSlots,
     BS_EMPTY = BS_FULL + 2,
-    BP_FULL = BS_EMPTY + 2, BP_EMPTY, BO_FULL, BO_EMPTY, BI_FULL,
+    BP_FULL = BS_EMPTY + 2, BO_FULL, BO_EMPTY, BI_FULL,
     BI_EMPTY = BI_FULL + kInfoSlots, BDRAIN = BI_EMPTY + kInfoSlots, NBARS
 };
 constexpr int kOffMisc = kOffBar + NBARS * 8;        // [0] tmem base, [1] abort flag
@@ -265,16 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar(BS_FULL + i), 1);
-            ptx::mbar_init(bar(BS_EMPTY + i), 4);
+            ptx::mbar_init(bar(BS_EMPTY + i), kSmWarps);
         }
         for (int i = 0; i < kInfoSlots; ++i) {
             ptx::mbar_init(bar(BI_FULL + i), 1);
-            ptx::mbar_init(bar(BI_EMPTY + i), 1 + 4 + kLoaderWarps);
+            ptx::mbar_init(bar(BI_EMPTY + i), 1 + kSmWarps + kLoaderWarps);
         }
-        ptx::mbar_init(bar(BP_FULL), 4);
-        ptx::mbar_init(bar(BP_EMPTY), 1);
+        ptx::mbar_init(bar(BP_FULL), kSmWarps);
         ptx::mbar_init(bar(BO_FULL), 1);
-        ptx::mbar_init(bar(BO_EMPTY), 4);
+        ptx::mbar_init(bar(BO_EMPTY), kSmWarps);
         ptx::mbar_init(bar(BDRAIN), 1);
         misc[1] = 0u;
         ptx::fence_mbar_init();
@@ -402,7 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::mma_commit(bar(BC_EMPTY + sl));
                 }
-                ptx::mma_commit(bar(BP_EMPTY));
                 if (in.b == in.nb - 1) {
                     ptx::mma_commit(bar(BO_FULL));
                     o_ph ^= 1;
@@ -418,10 +421,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    } else if (warp < 8) {
+    } else if (warp < kLoaderWarp0) {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
         // ---------------- softmax and output ----------------
+        // Two warps per TMEM lane quarter: warp set `hset` takes heads
+        // 32*hset..32*hset+31 of the scores and latent parts 2*hset, 2*hset+1 of
+        // the output.
+        const int sw = warp - 4;                   // 0..7
         const int sub = warp & 3;                  // TMEM lane quarter
+        const int hset = sw >> 2;                  // head half
+        const int h0 = kHh * hset;
         const int r = 32 * sub + lane;             // listed token / latent column
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * sub) << 16);
         float *m_s = reinterpret_cast<float *>(smem + kOffM);
@@ -429,24 +438,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *hs = reinterpret_cast<float *>(smem + kOffL);
         volatile uint32_t *flags = reinterpret_cast<volatile uint32_t *>(smem + kOffFlag);
         const float c = p.c_scale;
-        float l[kH];                               // this thread's partial sums per head
+        float l[kHh];                              // this thread's partial sums per head
         int blk = 0, agr = 0;
         uint32_t o_ph = 0;
         // every softmax warp passes each agreement barrier once per round and
         // leaves the loop on the same round
         auto agree = [&](uint32_t word) {
-            volatile uint32_t *f = flags + (agr & 1) * 4;
-            if (lane == 0) f[sub] = word;
+            volatile uint32_t *f = flags + (agr & 1) * kSmWarps;
+            if (lane == 0) f[sw] = word;
             ptx::named_bar_sync(3, kSmThreads);
-            const uint32_t all = f[0] | f[1] | f[2] | f[3];
+            uint32_t all = 0;
+#pragma unroll
+            for (int i = 0; i < kSmWarps; ++i) all |= f[i];
             ++agr;
             return all;
         };
-        // transpose-reduce of 64 per-head values over the warp: lane ends with
-        // heads 2*lane and 2*lane + 1
-        auto warp_reduce = [&](float (&v)[kH], bool is_max) {
+        // transpose-reduce of 32 per-head values over the warp: lane ends with
+        // head h0 + lane
+        auto warp_reduce = [&](float (&v)[kHh], bool is_max) {
 #pragma unroll
-            for (int w = 16, n = 32; w >= 1; w >>= 1, n >>= 1) {
+            for (int w = 16, n = 16; w >= 1; w >>= 1, n >>= 1) {
                 const bool up = (lane & w) != 0;
 #pragma unroll
                 for (int i = 0; i < n; ++i) {
@@ -460,11 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // v = 2^(v * c - m) in place against the reference maxima (shared, read
         // as broadcasts), 0 for a token that is not listed; true when some
         // exponent exceeds the rescale headroom
-        auto exponentiate = [&](float (&v)[kH], bool valid_row) {
+        auto exponentiate = [&](float (&v)[kHh], bool valid_row) {
             bool over = false;
-            const float4 *m4 = reinterpret_cast<const float4 *>(m_s);
+            const float4 *m4 = reinterpret_cast<const float4 *>(m_s + h0);
 #pragma unroll
-            for (int i = 0; i < kH / 4; ++i) {
+            for (int i = 0; i < kHh / 4; ++i) {
                 const float4 x = m4[i];
                 const float mq[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -476,25 +487,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return over;
         };
-        auto load_s = [&](int bs, float (&v)[kH]) {
-            uint32_t a[32], b2[32];
-            ptx::tmem_ld32(lane_base + bs * kH, a);
-            ptx::tmem_ld32(lane_base + bs * kH + 32, b2);
-            ptx::tmem_ld_wait2(a, b2);
+        auto load_s = [&](int bs, float (&v)[kHh]) {
+            uint32_t a[32];
+            ptx::tmem_ld32(lane_base + bs * kH + h0, a);
+            ptx::tmem_ld_wait(a);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                v[i] = __uint_as_float(a[i]);
-                v[32 + i] = __uint_as_float(b2[i]);
-            }
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(a[i]);
         };
-        bool bad = false;   // a wait of the previous round failed in this warp
-        // this thread's row of P (64 heads, BF16) in a 128-byte-swizzled tile
+        // this thread's half row of P (32 heads, BF16) in a 128-byte-swizzled tile
         const uint32_t prow = sP + r * 128;
         for (;;) {
             const int bs = blk & 1;
             const uint32_t bph = (blk >> 1) & 1;
             const int is = blk % kInfoSlots;
-            bool ok = !bad && wait_bar_warp(bar(BI_FULL + is), (blk / kInfoSlots) & 1, sy);
+            bool ok = wait_bar_warp(bar(BI_FULL + is), (blk / kInfoSlots) & 1, sy);
             BInfo in{};
             in.t = -1;
             if (ok) in = info[is];
@@ -506,9 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the block's probabilities, taken against the current reference
             // maxima before the warps agree (kept unless a rescale is needed);
             // defined on every path, so that none stays live across rounds
-            float pv[kH];
+            float pv[kHh];
 #pragma unroll
-            for (int h = 0; h < kH; ++h) pv[h] = 0.f;
+            for (int h = 0; h < kHh; ++h) pv[h] = 0.f;
             if (ok && !end) {
                 ok = wait_bar_warp(bar(BS_FULL + bs), bph, sy);
                 if (ok) {
@@ -516,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (in.b == 0) {
                         need = true;   // a new row: the reference maxima start over
 #pragma unroll
-                        for (int h = 0; h < kH; ++h) l[h] = 0.f;
+                        for (int h = 0; h < kHh; ++h) l[h] = 0.f;
                     } else {
                         load_s(bs, pv);
                         need = exponentiate(pv, valid) && valid;
@@ -530,45 +536,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // exact block maximum per head, new reference maxima, rescale
                 load_s(bs, pv);
 #pragma unroll
-                for (int h = 0; h < kH; ++h) pv[h] = valid ? pv[h] * c : -INFINITY;
+                for (int h = 0; h < kHh; ++h) pv[h] = valid ? pv[h] * c : -INFINITY;
                 warp_reduce(pv, true);
-                red[sub * kH + 2 * lane] = pv[0];
-                red[sub * kH + 2 * lane + 1] = pv[1];
+                red[sub * kH + h0 + lane] = pv[0];
                 ptx::named_bar_sync(3, kSmThreads);
                 if (sub == 0) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int h = 2 * lane + e;
-                        const float bm = fmaxf(fmaxf(red[h], red[kH + h]),
-                                               fmaxf(red[2 * kH + h], red[3 * kH + h]));
-                        const float mo = in.b == 0 ? -INFINITY : m_s[h];
-                        const float mn = fmaxf(mo, bm);
-                        hs[h] = (mn == -INFINITY) ? 1.f : ptx::ex2_approx(mo - mn);
-                        m_s[h] = mn;
-                    }
+                    const int h = h0 + lane;
+                    const float bm = fmaxf(fmaxf(red[h], red[kH + h]),
+                                           fmaxf(red[2 * kH + h], red[3 * kH + h]));
+                    const float mo = in.b == 0 ? -INFINITY : m_s[h];
+                    const float mn = fmaxf(mo, bm);
+                    hs[h] = (mn == -INFINITY) ? 1.f : ptx::ex2_approx(mo - mn);
+                    m_s[h] = mn;
                 }
                 ptx::named_bar_sync(3, kSmThreads);
-                // the previous block's output MMAs must be complete before O^T
-                // is rescaled and before P is overwritten
-                bad = !wait_bar_warp(bar(BP_EMPTY), (blk & 1) ^ 1, sy);
-                if (in.b > 0 && !bad) {
+                if (in.b > 0) {
                     bool scale_o = false;
 #pragma unroll
-                    for (int h = 0; h < kH; ++h) {
-                        const float a = hs[h];
+                    for (int h = 0; h < kHh; ++h) {
+                        const float a = hs[h0 + h];
                         l[h] *= a;
-                        scale_o |= a != 1.f;
                     }
+#pragma unroll
+                    for (int h = 0; h < kH; ++h) scale_o |= hs[h] != 1.f;
                     if (scale_o) {
-                        // every PV MMA of the earlier blocks has completed (their
-                        // completion precedes this block's scores); the factors
-                        // are re-read per part rather than held in registers
+                        // the factors are re-read per part rather than held in
+                        // registers
                         const volatile float *hsv = hs;
 #pragma unroll 1
-                        for (int sl = 0; sl < kOParts; ++sl) {
+                        for (int op = 2 * hset; op < 2 * hset + 2; ++op) {
 #pragma unroll
                             for (int half = 0; half < 2; ++half) {
-                                const uint32_t ta = lane_base + 128 + sl * kH + half * 32;
+                                const uint32_t ta = lane_base + 128 + op * kH + half * 32;
                                 uint32_t ov[32];
                                 ptx::tmem_ld32(ta, ov);
                                 ptx::tmem_ld_wait(ov);
@@ -585,68 +584,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // across the rescale)
                 load_s(bs, pv);
                 exponentiate(pv, valid);
-            } else {
-                bad = !wait_bar_warp(bar(BP_EMPTY), (blk & 1) ^ 1, sy);
             }
-            // P[r][h] (BF16, eight heads per 16-byte piece) and the partial sums
-            if (!bad) {
+            // P[r][h] (BF16, eight heads per 16-byte piece), then the partial sums.
+            // This block's scores have landed, so every earlier MMA has completed
+            // (a commit's arrival covers all earlier MMAs of the issuing thread):
+            // the previous block's output MMAs no longer read P, and O^T above
+            // was final when rescaled.
+            {
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(BS_EMPTY + bs));
 #pragma unroll
-                for (int j = 0; j < kH / 8; ++j) {
+                for (int j = 0; j < kHh / 8; ++j) {
                     uint32_t w[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int h = 8 * j + 2 * i;
-                        l[h] += pv[h];
-                        l[h + 1] += pv[h + 1];
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(pv[h], pv[h + 1]);
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(pv[8 * j + 2 * i], pv[8 * j + 2 * i + 1]);
                         w[i] = *reinterpret_cast<const uint32_t *>(&b2);
                     }
-                    ptx::st_shared_v4(prow + ((j ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+                    const int piece = 4 * hset + j;
+                    ptx::st_shared_v4(prow + ((piece ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(BP_FULL));
+#pragma unroll
+                for (int h = 0; h < kHh; ++h) l[h] += pv[h];
             }
             if (in.b == in.nb - 1) {
                 // the row's output once its last PV MMAs have landed
-                const bool ok2 = !bad && wait_bar_warp(bar(BO_FULL), o_ph, sy);
+                const bool ok2 = wait_bar_warp(bar(BO_FULL), o_ph, sy);
                 o_ph ^= 1;
                 if (agree(ok2 ? 0u : 1u) & 1u) break;
                 ptx::tc_fence_after();
-                float v[kH];
+                float v[kHh];
 #pragma unroll
-                for (int h = 0; h < kH; ++h) v[h] = l[h];
+                for (int h = 0; h < kHh; ++h) v[h] = l[h];
                 warp_reduce(v, false);
-                red[sub * kH + 2 * lane] = v[0];
-                red[sub * kH + 2 * lane + 1] = v[1];
+                red[sub * kH + h0 + lane] = v[0];
                 ptx::named_bar_sync(3, kSmThreads);
                 if (sub == 0) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int h = 2 * lane + e;
-                        const float L = (red[h] + red[kH + h]) + (red[2 * kH + h] + red[3 * kH + h]);
-                        hs[h] = L > 0.f ? 1.f / L : 0.f;
-                        p.lse[static_cast<int64_t>(in.t) * kH + h] =
-                            L > 0.f ? (m_s[h] + log2f(L)) * 0.69314718055994531f : -INFINITY;
-                    }
+                    const int h = h0 + lane;
+                    const float L = (red[h] + red[kH + h]) + (red[2 * kH + h] + red[3 * kH + h]);
+                    hs[h] = L > 0.f ? 1.f / L : 0.f;
+                    p.lse[static_cast<int64_t>(in.t) * kH + h] =
+                        L > 0.f ? (m_s[h] + log2f(L)) * 0.69314718055994531f : -INFINITY;
                 }
                 ptx::named_bar_sync(3, kSmThreads);
                 uint16_t *orow = p.o + static_cast<int64_t>(in.t) * kH * kDc + r;
 #pragma unroll 1
-                for (int sl = 0; sl < kOParts; ++sl) {
+                for (int op = 2 * hset; op < 2 * hset + 2; ++op) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t ov[32];
-                        ptx::tmem_ld32(lane_base + 128 + sl * kH + half * 32, ov);
+                        ptx::tmem_ld32(lane_base + 128 + op * kH + half * 32, ov);
                         ptx::tmem_ld_wait(ov);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int h = half * 32 + i;
                             const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(ov[i]) * hs[h]);
-                            orow[static_cast<int64_t>(h) * kDc + sl * 128] =
+                            orow[static_cast<int64_t>(h) * kDc + op * 128] =
                                 *reinterpret_cast<const uint16_t *>(&bv);
                         }
                     }
@@ -663,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Each slot has its own pair of warps, so the four slots of a block
         // refill independently as the output MMAs free them: a pair waits only
         // for its own copies (then a proxy fence and its arrival on the slot).
-        const int sl = (warp - 8) >> 1;                   // the slot of this pair
-        const int t64 = ((warp - 8) & 1) * 32 + lane;     // 0..63 within the pair
+        const int sl = (warp - kLoaderWarp0) >> 1;                 // the slot of this pair
+        const int t64 = ((warp - kLoaderWarp0) & 1) * 32 + lane;   // 0..63 within the pair
         const int k = t64 & 15;                           // 16-byte piece of the slot's 256 bytes
         const char *kvb = reinterpret_cast<const char *>(p.kv) + sl * 256 + k * 16;
         const uint32_t dst_slot = sC + sl * kPair + (k >> 3) * kChunk;
