@@ -442,8 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int blk = 0, agr = 0;
         uint32_t o_ph = 0;
         // every softmax warp passes each agreement barrier once per round and
-        // leaves the loop on the same round
+        // leaves the loop on the same round; `word` is uniform in a warp.  A
+        // barrier reduction first says whether any warp has a nonzero word (the
+        // common round ends there); only then are the words exchanged.
         auto agree = [&](uint32_t word) {
+            if (!ptx::named_bar_or(4, kSmThreads, word != 0u)) return 0u;
             volatile uint32_t *f = flags + (agr & 1) * kSmWarps;
             if (lane == 0) f[sw] = word;
             ptx::named_bar_sync(3, kSmThreads);

@@ -166,7 +166,8 @@ struct Params {
 
 // 2 relu(x), exactly (x + |x| is 2x or +0), as one add with an absolute-value
 // operand on the FMA pipe rather than a max on the ALU pipe; the head weights are
-// staged halved to match.
+// staged halved to match.  (Only an accumulator of -inf, which needs inputs whose
+// products overflow FP32, would differ: NaN here, 0 from a max.)
 __device__ __forceinline__ float twice_relu(float x) { return __fadd_rn(x, fabsf(x)); }
 
 // Orderable key of a score: larger float -> larger key; -0 folded into +0.
