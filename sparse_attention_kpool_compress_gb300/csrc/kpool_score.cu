@@ -233,9 +233,26 @@ __device__ __forceinline__ int pool_tiles_of(const TileInfo &ti, int QT, int kp)
 
 __device__ __forceinline__ void group_bar(int g) { ptx::named_bar_sync(2 + g, kGroupThreads); }
 
+// A selection group of NW warps: one of the four groups of four warps, or all
+// sixteen epilogue warps at once (a lone query).  Its barrier and the slots of
+// its scratch words gs (per-warp arrays and scalars; with NW = 16 the scratch
+// spans all four groups' areas).
+template <int NW>
+__device__ __forceinline__ void sel_bar(int g)
+{
+    if constexpr (NW == kGroupWarps) group_bar(g);
+    else ptx::named_bar_sync(1, kEpiThreads);
+}
+template <int NW>
+struct Gs {
+    static constexpr int kMin = 0, kMax = NW, kCnt = 2 * NW, kScal = 3 * NW;
+    static constexpr int kA = 3 * NW + 4, kB = 4 * NW + 4, kCtr = 5 * NW + 4;
+};
+static_assert(Gs<kEpiWarps>::kCtr < kGroups * 32, "wide selection scratch");
+
 // Radix search (DeepSelect-style, 8-bit digits) for the k-th largest of
 // keyf(e) over the entries e < n with partf(e), by one selection group
-// (kGroupThreads threads).
+// (32 NW threads).
 // Digits start at the highest bit where the smallest and largest
 // participating key differ, so the first histogram is spread.  Results:
 //   kth    the k-th largest key, or (edge) the lower edge of the digit bin
@@ -243,7 +260,7 @@ __device__ __forceinline__ void group_bar(int g) { ptx::named_bar_sync(2 + g, kG
 //          keeping everything at or above the edge keeps <= k + slack entries;
 //   above  participants with key above the bin / above kth;
 //   inbin  participants in that bin / equal to kth.
-template <class KeyFn, class PartFn>
+template <int NW, class KeyFn, class PartFn>
 __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, bool allow_edge,
                           int slack, int g, int gtid, int *hist, int *gs, uint32_t &kth,
                           int &above, int &inbin, bool &edge)
@@ -251,7 +268,7 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
     const int lane = gtid & 31, gw = gtid >> 5;
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
     int cnt = 0;
-    for (int e = gtid; e < n; e += kGroupThreads) {
+    for (int e = gtid; e < n; e += (32 * NW)) {
         if (partf(e)) {
             const uint32_t key = keyf(e);
             kmin = min(kmin, key);
@@ -263,19 +280,19 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
     kmax = __reduce_max_sync(kFull, kmax);
     cnt = __reduce_add_sync(kFull, cnt);
     if (lane == 0) {
-        gs[gw] = static_cast<int>(kmin);
-        gs[4 + gw] = static_cast<int>(kmax);
-        gs[8 + gw] = cnt;
+        gs[Gs<NW>::kMin + gw] = static_cast<int>(kmin);
+        gs[Gs<NW>::kMax + gw] = static_cast<int>(kmax);
+        gs[Gs<NW>::kCnt + gw] = cnt;
     }
-    group_bar(g);
+    sel_bar<NW>(g);
     kmin = 0xFFFFFFFFu;
     kmax = 0u;
     cnt = 0;
 #pragma unroll
-    for (int w = 0; w < kGroupWarps; ++w) {
-        kmin = min(kmin, static_cast<uint32_t>(gs[w]));
-        kmax = max(kmax, static_cast<uint32_t>(gs[4 + w]));
-        cnt += gs[8 + w];
+    for (int w = 0; w < NW; ++w) {
+        kmin = min(kmin, static_cast<uint32_t>(gs[Gs<NW>::kMin + w]));
+        kmax = max(kmax, static_cast<uint32_t>(gs[Gs<NW>::kMax + w]));
+        cnt += gs[Gs<NW>::kCnt + w];
     }
     above = 0;
     if (kmin == kmax) {
@@ -290,15 +307,15 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
     while (true) {
         const int lo = max(hi - 7, 0);
         const uint32_t dmask = (2u << (hi - lo)) - 1u;
-        for (int i = gtid; i < 256; i += kGroupThreads) hist[i] = 0;
-        group_bar(g);
-        for (int e = gtid; e < n; e += kGroupThreads) {
+        for (int i = gtid; i < 256; i += (32 * NW)) hist[i] = 0;
+        sel_bar<NW>(g);
+        for (int e = gtid; e < n; e += (32 * NW)) {
             if (!partf(e)) continue;
             const uint32_t key = keyf(e);
             if (hi == 31 || (key >> (hi + 1)) == (prefix >> (hi + 1)))
                 atomicAdd(&hist[(key >> lo) & dmask], 1);
         }
-        group_bar(g);
+        sel_bar<NW>(g);
         if (gw == 0) {
             int b[8];
             int local = 0;
@@ -317,15 +334,15 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
 #pragma unroll
             for (int i = 7; i >= 0; --i) {
                 if (cum < kr && cum + b[i] >= kr) {
-                    gs[12] = lane * 8 + i;
-                    gs[13] = cum;
-                    gs[14] = b[i];
+                    gs[Gs<NW>::kScal] = lane * 8 + i;
+                    gs[Gs<NW>::kScal + 1] = cum;
+                    gs[Gs<NW>::kScal + 2] = b[i];
                 }
                 cum += b[i];
             }
         }
-        group_bar(g);
-        const int d = gs[12], cum = gs[13], hb = gs[14];
+        sel_bar<NW>(g);
+        const int d = gs[Gs<NW>::kScal], cum = gs[Gs<NW>::kScal + 1], hb = gs[Gs<NW>::kScal + 2];
         prefix |= static_cast<uint32_t>(d) << lo;
         kr -= cum;
         above += cum;
@@ -350,6 +367,7 @@ __device__ void radix_kth(int n, int k, const KeyFn &keyf, const PartFn &partf, 
 // mode (exact = false) it may keep up to k + slack entries: all those at or
 // above a digit-bin edge.  Returns the number kept and writes to *thr_out the
 // key a later candidate (higher pool index) must exceed to possibly enter.
+template <int NW = kGroupWarps>
 __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int slack, int g,
                             int gtid, int *hist, int *gs, uint32_t *thr_out)
 {
@@ -358,7 +376,7 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
     uint32_t kth;
     int above, inbin;
     bool edge;
-    radix_kth(n, k, [&](int e) { return fkey(cs[e]); }, [](int) { return true; }, !exact, slack, g,
+    radix_kth<NW>(n, k, [&](int e) { return fkey(cs[e]); }, [](int) { return true; }, !exact, slack, g,
               gtid, hist, gs, kth, above, inbin, edge);
     // ties at the k-th score: keep the lowest pool indices among them
     uint32_t ithr = 0xFFFFFFFFu;   // keep tied entries with ci <= ithr
@@ -368,15 +386,15 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
         uint32_t ik;
         int iab, iin;
         bool ied;
-        group_bar(g);   // gs reuse
-        radix_kth(n, need, [&](int e) { return ~static_cast<uint32_t>(ci[e]); },
+        sel_bar<NW>(g);   // gs reuse
+        radix_kth<NW>(n, need, [&](int e) { return ~static_cast<uint32_t>(ci[e]); },
                   [&](int e) { return fkey(cs[e]) == kth; }, false, 0, g, gtid, hist, gs, ik, iab,
                   iin, ied);
         ithr = ~ik;
     }
-    group_bar(g);   // gs reused below
+    sel_bar<NW>(g);   // gs reused below
     const int chunks = (n + 31) / 32;
-    const int per = ((chunks + kGroupWarps - 1) / kGroupWarps) * 32;
+    const int per = ((chunks + NW - 1) / NW) * 32;
     const int r0 = gw * per, r1 = min(n, r0 + per);
     int cnt = 0;
     for (int c = r0; c < r1; c += 32) {
@@ -399,16 +417,16 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
         }
         cnt += __popc(kb);
     }
-    if (lane == 0) gs[16 + gw] = cnt;
-    group_bar(g);
+    if (lane == 0) gs[Gs<NW>::kA + gw] = cnt;
+    sel_bar<NW>(g);
     int total = 0, mybase = 0;
 #pragma unroll
-    for (int w = 0; w < kGroupWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
         if (w == gw) mybase = total;
-        total += gs[16 + w];
+        total += gs[Gs<NW>::kA + w];
     }
     // move each later warp's kept block down behind the earlier ones, in order
-    for (int w = 1; w < kGroupWarps; ++w) {
+    for (int w = 1; w < NW; ++w) {
         if (gw == w) {
             for (int c = 0; c < cnt; c += 32) {
                 const int i = c + lane;
@@ -425,10 +443,10 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
                 }
             }
         }
-        group_bar(g);
+        sel_bar<NW>(g);
     }
     if (gtid == 0) *thr_out = edge ? (kth > 0 ? kth - 1u : 0u) : kth;
-    group_bar(g);
+    sel_bar<NW>(g);
     return total;
 }
 
@@ -437,21 +455,22 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
 // index ci - pool_base < 32 * words).  The bitmap lives in ci[n .. n+words)
 // and the per-word prefix counts in cs[n .. n+words) (the free tail of the
 // query's candidate area; words <= capacity - n).  One group.
+template <int NW = kGroupWarps>
 __device__ void group_rank_store(float *cs, int *ci, int n, int pool_base, int words, int g,
                                  int gtid, int *gs, int32_t *out_idx, float *out_score)
 {
     const int lane = gtid & 31, gw = gtid >> 5;
     uint32_t *bm = reinterpret_cast<uint32_t *>(ci + n);
     int *pf = reinterpret_cast<int *>(cs + n);
-    for (int w = gtid; w < words; w += kGroupThreads) bm[w] = 0u;
-    group_bar(g);
-    for (int e = gtid; e < n; e += kGroupThreads) {
+    for (int w = gtid; w < words; w += (32 * NW)) bm[w] = 0u;
+    sel_bar<NW>(g);
+    for (int e = gtid; e < n; e += (32 * NW)) {
         const int j = ci[e] - pool_base;
         atomicOr(&bm[j >> 5], 1u << (j & 31));
     }
-    group_bar(g);
+    sel_bar<NW>(g);
     // exclusive prefix of popcounts over words: each thread a contiguous run
-    const int per = (words + kGroupThreads - 1) / kGroupThreads;
+    const int per = (words + (32 * NW) - 1) / (32 * NW);
     const int w0 = gtid * per, w1 = min(words, w0 + per);
     int local = 0;
     for (int w = w0; w < w1; ++w) local += __popc(bm[w]);
@@ -461,16 +480,16 @@ __device__ void group_rank_store(float *cs, int *ci, int n, int pool_base, int w
         const int o = __shfl_up_sync(kFull, incl, off);
         if (lane >= off) incl += o;
     }
-    if (lane == 31) gs[20 + gw] = incl;
-    group_bar(g);
+    if (lane == 31) gs[Gs<NW>::kB + gw] = incl;
+    sel_bar<NW>(g);
     int run = incl - local;
-    for (int w = 0; w < gw; ++w) run += gs[20 + w];
+    for (int w = 0; w < gw; ++w) run += gs[Gs<NW>::kB + w];
     for (int w = w0; w < w1; ++w) {
         pf[w] = run;
         run += __popc(bm[w]);
     }
-    group_bar(g);
-    for (int e = gtid; e < n; e += kGroupThreads) {
+    sel_bar<NW>(g);
+    for (int e = gtid; e < n; e += (32 * NW)) {
         const int j = ci[e] - pool_base;
         const int r = pf[j >> 5] + __popc(bm[j >> 5] & ((1u << (j & 31)) - 1u));
         out_idx[r] = ci[e];
@@ -483,13 +502,14 @@ __device__ void group_rank_store(float *cs, int *ci, int n, int pool_base, int w
 // n <= k, to out_idx/out_score in ascending pool order and returns how many
 // it wrote.  One selection group: a radix search for the k-th key, then two
 // ordered passes (counts per warp, then ballot-ranked writes).
+template <int NW = kGroupWarps>
 __device__ int group_select_direct(const float *dq, int n, int k, int pool_base, int g, int gtid,
                                    int *hist, int *gs, int32_t *out_idx, float *out_score)
 {
     const int lane = gtid & 31, gw = gtid >> 5;
     const unsigned lt = (1u << lane) - 1u;
     if (n <= k) {
-        for (int e = gtid; e < n; e += kGroupThreads) {
+        for (int e = gtid; e < n; e += (32 * NW)) {
             out_idx[e] = pool_base + e;
             out_score[e] = dq[e];
         }
@@ -498,13 +518,13 @@ __device__ int group_select_direct(const float *dq, int n, int k, int pool_base,
     uint32_t kth;
     int above, inbin;
     bool edge;
-    radix_kth(n, k, [&](int e) { return fkey(dq[e]); }, [](int) { return true; }, false, 0, g,
+    radix_kth<NW>(n, k, [&](int e) { return fkey(dq[e]); }, [](int) { return true; }, false, 0, g,
               gtid, hist, gs, kth, above, inbin, edge);
     // edge: the bin holds exactly the entries still needed -> keep key >= kth;
     // otherwise keep key > kth and the first `need` entries equal to it
     const int need = edge ? 0 : k - above;
-    group_bar(g);   // gs reuse
-    const int per_w = ((n + kGroupThreads - 1) / kGroupThreads) * 32;
+    sel_bar<NW>(g);   // gs reuse
+    const int per_w = ((n + (32 * NW) - 1) / (32 * NW)) * 32;
     const int r0 = gw * per_w, r1 = min(n, r0 + per_w);
     int cgt = 0, ceq = 0;
     for (int c = r0; c < r1; c += 32) {
@@ -514,14 +534,14 @@ __device__ int group_select_direct(const float *dq, int n, int k, int pool_base,
         ceq += __popc(__ballot_sync(kFull, e < r1 && !edge && key == kth));
     }
     if (lane == 0) {
-        gs[16 + gw] = cgt;
-        gs[20 + gw] = ceq;
+        gs[Gs<NW>::kA + gw] = cgt;
+        gs[Gs<NW>::kB + gw] = ceq;
     }
-    group_bar(g);
+    sel_bar<NW>(g);
     int base_gt = 0, base_eq = 0;
     for (int w = 0; w < gw; ++w) {
-        base_gt += gs[16 + w];
-        base_eq += gs[20 + w];
+        base_gt += gs[Gs<NW>::kA + w];
+        base_eq += gs[Gs<NW>::kB + w];
     }
     int pos = base_gt + min(base_eq, need);
     int eq_seen = base_eq;
@@ -542,24 +562,25 @@ __device__ int group_select_direct(const float *dq, int n, int k, int pool_base,
         pos += __popc(bk);
         eq_seen += __popc(beq);
     }
-    group_bar(g);   // gs reuse by the caller
+    sel_bar<NW>(g);   // gs reuse by the caller
     return k;
 }
 
 // Ascending sort of cs/ci[0..n) by pool index (ci), bitonic over the next
 // power of two (pad entries carry INT_MAX), by one group.  n2 <= capacity.
+template <int NW = kGroupWarps>
 __device__ void group_sort_by_pool(float *cs, int *ci, int n, int g, int gtid)
 {
     int n2 = 1;
     while (n2 < n) n2 <<= 1;
-    for (int i = n + gtid; i < n2; i += kGroupThreads) {
+    for (int i = n + gtid; i < n2; i += (32 * NW)) {
         ci[i] = 0x7FFFFFFF;
         cs[i] = -INFINITY;
     }
-    group_bar(g);
+    sel_bar<NW>(g);
     for (int kk = 2; kk <= n2; kk <<= 1) {
         for (int j = kk >> 1; j > 0; j >>= 1) {
-            for (int i = gtid; i < n2; i += kGroupThreads) {
+            for (int i = gtid; i < n2; i += (32 * NW)) {
                 const int ixj = i ^ j;
                 if (ixj > i) {
                     const int a = ci[i], b = ci[ixj];
@@ -573,7 +594,7 @@ __device__ void group_sort_by_pool(float *cs, int *ci, int n, int g, int gtid)
                     }
                 }
             }
-            group_bar(g);
+            sel_bar<NW>(g);
         }
     }
 }
@@ -583,6 +604,7 @@ __device__ void group_sort_by_pool(float *cs, int *ci, int n, int g, int gtid)
 // INT_MAX and score -inf), written to cs/ci[0..) in any order; all real
 // entries when at most k of the n_real are real.  One group.  Returns the
 // number written (min(k, n_real)).
+template <int NW = kGroupWarps>
 __device__ int group_select_into(const float *sc, const int32_t *ix, int n, int k, int n_real,
                                  float *cs, int *ci, int g, int gtid, int *hist, int *gs)
 {
@@ -592,23 +614,23 @@ __device__ int group_select_into(const float *sc, const int32_t *ix, int n, int 
     bool edge = false;
     if (!all) {
         int above, inbin;
-        radix_kth(n, k, [&](int e) { return fkey(__ldcg(sc + e)); }, [](int) { return true; },
+        radix_kth<NW>(n, k, [&](int e) { return fkey(__ldcg(sc + e)); }, [](int) { return true; },
                   false, 0, g, gtid, hist, gs, kth, above, inbin, edge);
         if (!edge && above + inbin > k) {
             uint32_t ik;
             int iab, iin;
             bool ied;
-            group_bar(g);   // gs reuse
-            radix_kth(n, k - above, [&](int e) { return ~static_cast<uint32_t>(__ldcg(ix + e)); },
+            sel_bar<NW>(g);   // gs reuse
+            radix_kth<NW>(n, k - above, [&](int e) { return ~static_cast<uint32_t>(__ldcg(ix + e)); },
                       [&](int e) { return fkey(__ldcg(sc + e)) == kth; }, false, 0, g, gtid, hist,
                       gs, ik, iab, iin, ied);
             ithr = ~ik;
         }
     }
-    group_bar(g);
-    if (gtid == 0) gs[24] = 0;
-    group_bar(g);
-    for (int c = 0; c < n; c += kGroupThreads) {
+    sel_bar<NW>(g);
+    if (gtid == 0) gs[Gs<NW>::kCtr] = 0;
+    sel_bar<NW>(g);
+    for (int c = 0; c < n; c += (32 * NW)) {
         const int e = c + gtid;
         bool keep = false;
         float sv = 0.f;
@@ -623,7 +645,7 @@ __device__ int group_select_into(const float *sc, const int32_t *ix, int n, int 
         }
         const unsigned kb = __ballot_sync(kFull, keep);
         int base = 0;
-        if (lane == 0 && kb != 0u) base = atomicAdd(&gs[24], __popc(kb));
+        if (lane == 0 && kb != 0u) base = atomicAdd(&gs[Gs<NW>::kCtr], __popc(kb));
         base = __shfl_sync(kFull, base, 0);
         if (keep) {
             const int d = base + __popc(kb & ((1u << lane) - 1u));
@@ -631,9 +653,9 @@ __device__ int group_select_into(const float *sc, const int32_t *ix, int n, int 
             ci[d] = iv;
         }
     }
-    group_bar(g);
-    const int total = gs[24];
-    group_bar(g);   // gs reuse
+    sel_bar<NW>(g);
+    const int total = gs[Gs<NW>::kCtr];
+    sel_bar<NW>(g);   // gs reuse
     return total;
 }
 
@@ -652,22 +674,31 @@ __device__ __noinline__ bool split_unit_end(const TileInfo *tu, int nq, int QT, 
     const int splits = tu->splits;
     const int uk = tu->k;
     const int64_t tbase = static_cast<int64_t>(tu->slot_base) * QT;
-    for (int q = g; q < nq; q += kGroups) {
+    // a lone query takes all sixteen warps (one wide group), else each group
+    // takes its own queries
+    const bool wide = nq == 1;
+    int *hist0 = hist - g * 256, *gs0 = gs - g * 32;
+    auto unit_out = [&](auto nw, int q, int gg, int tid, int *hh, int *gss) {
+        constexpr int NW = decltype(nw)::value;
         int n = qcnt[q];
         float *csq = cs + q * C;
         int *ciq = ci + q * C;
         if (n > Kp) {
-            group_select(csq, ciq, n, Kp, true, 0, g, gtid, hist, gs, &thr_s[q]);
+            group_select<NW>(csq, ciq, n, Kp, true, 0, gg, tid, hh, gss, &thr_s[q]);
             n = Kp;
         }
         const int64_t li = tbase + q * splits + uk;
-        for (int e = gtid; e < Kp; e += kGroupThreads) {
+        for (int e = tid; e < Kp; e += 32 * NW) {
             const bool real = e < n;
             part_idx[li * Kp + e] = real ? ciq[e] : 0x7FFFFFFF;
             part_score[li * Kp + e] = real ? csq[e] : -INFINITY;
         }
-        if (gtid == 0) part_cnt[li] = n;
-    }
+        if (tid == 0) part_cnt[li] = n;
+    };
+    if (wide) unit_out(std::integral_constant<int, kEpiWarps>{}, 0, 0, etid, hist0, gs0);
+    else
+        for (int q = g; q < nq; q += kGroups)
+            unit_out(std::integral_constant<int, kGroupWarps>{}, q, g, gtid, hist, gs);
     __threadfence();
     ptx::named_bar_sync(1, kEpiThreads);
     if (etid == 0) *flag = atomicAdd(tile_ctr + tu->tile, 1) == splits - 1 ? 1u : 0u;
@@ -675,15 +706,21 @@ __device__ __noinline__ bool split_unit_end(const TileInfo *tu, int nq, int QT, 
     const bool last = *flag != 0u;
     if (last) {
         __threadfence();
-        for (int q = g; q < nq; q += kGroups) {
+        auto merge = [&](auto nw, int q, int gg, int tid, int *hh, int *gss) {
+            constexpr int NW = decltype(nw)::value;
             const int64_t l0 = tbase + q * splits;
             int n_real = 0;
             for (int u = 0; u < splits; ++u) n_real += __ldcg(part_cnt + l0 + u);
-            const int n = group_select_into(part_score + l0 * Kp, part_idx + l0 * Kp, splits * Kp,
-                                            Kp, n_real, cs + q * C, ci + q * C, g, gtid, hist, gs);
-            if (gtid == 0) qcnt[q] = n;
-            group_bar(g);
-        }
+            const int n = group_select_into<NW>(part_score + l0 * Kp, part_idx + l0 * Kp,
+                                                splits * Kp, Kp, n_real, cs + q * C, ci + q * C,
+                                                gg, tid, hh, gss);
+            if (tid == 0) qcnt[q] = n;
+            sel_bar<NW>(gg);
+        };
+        if (wide) merge(std::integral_constant<int, kEpiWarps>{}, 0, 0, etid, hist0, gs0);
+        else
+            for (int q = g; q < nq; q += kGroups)
+                merge(std::integral_constant<int, kGroupWarps>{}, q, g, gtid, hist, gs);
     }
     return last;
 }
@@ -968,6 +1005,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gtid = etid - g * kGroupThreads;
         int *hist = reinterpret_cast<int *>(smem + L.hist_off) + g * 256;
         int *gs = reinterpret_cast<int *>(smem + L.scr_off) + g * 32;
+        // the wide group (all sixteen warps, a lone query) uses group 0's histogram
+        // and every group's scratch words
+        int *hist0 = reinterpret_cast<int *>(smem + L.hist_off);
+        int *gs0 = reinterpret_cast<int *>(smem + L.scr_off);
         int *qcnt = reinterpret_cast<int *>(smem + L.cnt_off);   // candidates per query
         uint32_t *thr_s = reinterpret_cast<uint32_t *>(smem + L.thr_off);
         float *cs = reinterpret_cast<float *>(smem + L.cs_off);
@@ -1315,11 +1356,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if ((m % Gq) == Gq - 1 && m != nquad - 1) {
                             ptx::named_bar_sync(1, kEpiThreads);
                             if (qcnt[0] > room_q) {
-                                if (g == 0) {
-                                    const int nn = group_select(cs, ci, qcnt[0], Kp, false, slack, 0,
-                                                                gtid, hist, gs, &thr_s[0]);
-                                    if (gtid == 0) qcnt[0] = nn;
-                                }
+                                // all sixteen warps prune the lone query's area
+                                const int nn = group_select<kEpiWarps>(cs, ci, qcnt[0], Kp, false,
+                                                                       slack, 0, etid, hist0, gs0,
+                                                                       &thr_s[0]);
+                                if (etid == 0) qcnt[0] = nn;
                                 ptx::named_bar_sync(1, kEpiThreads);
                                 thr0 = thr_s[0];
                             }
@@ -1361,7 +1402,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.pool_score[row + e] = -INFINITY;
                 }
             }
-            for (int q = g; q < nq && emit && !direct; q += kGroups) {
+            bool lone_done = false;
+            if constexpr (kQuad) {
+                if (nq == 1 && emit && !direct) {
+                    // a lone query: all sixteen warps select and store it
+                    constexpr int NW = kEpiWarps;
+                    int n = qcnt[0];
+                    if (n > Kp) {
+                        group_select<NW>(cs, ci, n, Kp, true, 0, 0, etid, hist0, gs0, &thr_s[0]);
+                        n = Kp;
+                    }
+                    const int64_t row = static_cast<int64_t>(t.t0) * Kp;
+                    const int nc_q = min((tau0 + 1) / p.kp, t.pool_count);
+                    const int words = (nc_q + 31) / 32;
+                    if (words <= QT * C - n) {
+                        group_rank_store<NW>(cs, ci, n, t.pool_base, words, 0, etid, gs0,
+                                             p.pool_idx + row, p.pool_score + row);
+                    } else {
+                        group_sort_by_pool<NW>(cs, ci, n, 0, etid);
+                        for (int e = etid; e < n; e += kEpiThreads) {
+                            p.pool_idx[row + e] = ci[e];
+                            p.pool_score[row + e] = cs[e];
+                        }
+                    }
+                    for (int e = n + etid; e < Kp; e += kEpiThreads) {
+                        p.pool_idx[row + e] = -1;
+                        p.pool_score[row + e] = -INFINITY;
+                    }
+                    lone_done = true;
+                }
+            }
+            for (int q = g; q < nq && emit && !direct && !lone_done; q += kGroups) {
                 int n = qcnt[q];
                 float *csq = cs + q * C;
                 int *ciq = ci + q * C;
