@@ -1164,6 +1164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int npt = t.i1 - t.i0;
             auto tiles = [&](auto direct_tag) {
             constexpr bool kDirect = decltype(direct_tag)::value;
+            int gleft = G;   // tiles to the next capacity check (a countdown, not i % G)
             for (int i = 0; i < npt; ++i) {
                 PT_MARK(1);
                 aborted |= !wait_bar_warp(bar(BTM_FULL + acc), acc_ph, sy);
@@ -1283,7 +1284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 PT_MARK(4);
-                if ((i % G) == G - 1 && i != npt - 1) {
+                const bool check = --gleft == 0;
+                if (check) gleft = G;
+                if (check && i != npt - 1) {
                     // capacity check: compact queries past the room, plus those past
                     // half of it, each group on its own queries in parallel
                     ptx::named_bar_sync(1, kEpiThreads);
