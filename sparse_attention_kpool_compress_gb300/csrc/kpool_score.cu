@@ -178,6 +178,18 @@ __device__ __forceinline__ uint32_t fkey(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The smallest score whose key exceeds k, so that fkey(s) > k exactly when
+// s >= pass_floor(k) for every score s (never NaN; -0 folded into +0): -inf
+// when every score passes, NaN when none does.  One float compare per pool
+// then replaces the key computation.
+__device__ __forceinline__ float pass_floor(uint32_t k)
+{
+    if (k < 0x007FFFFFu) return -INFINITY;                    // below the key of -inf
+    if (k >= 0xFF800000u) return __uint_as_float(0x7FC00000u);  // at or above +inf's key
+    const uint32_t e = k + 1u;
+    return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
+}
+
 struct Sync {
     volatile uint32_t *abort_flag;
     int *status;
@@ -1091,11 +1103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
 
-            uint32_t thr[QS];
+            float thf[QS];   // pass_floor of each query's threshold key
             int nc[QS];
 #pragma unroll
             for (int j = 0; j < QS; ++j) {
-                thr[j] = 0u;
+                thf[j] = -INFINITY;
                 nc[j] = min((tau0 + qbase + j + 1) / p.kp, t.pool_count);
             }
             bool aborted = false;
@@ -1269,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < QS; ++j) {
                         const int qi = qbase + j;
-                        const bool ps = (qi < nq) && (pool_local < nc[j]) && (fkey(s[j]) > thr[j]);
+                        const bool ps = (qi < nq) && (pool_local < nc[j]) && s[j] >= thf[j];
                         const unsigned bal = __ballot_sync(kFull, ps);
                         if (bal != 0u) {
                             int base = 0;
@@ -1303,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ptx::named_bar_sync(1, kEpiThreads);
 #pragma unroll
-                        for (int j = 0; j < QS; ++j) thr[j] = thr_s[qbase + j];
+                        for (int j = 0; j < QS; ++j) thf[j] = pass_floor(thr_s[qbase + j]);
                     }
                     PT_MARK(5);
                 }
