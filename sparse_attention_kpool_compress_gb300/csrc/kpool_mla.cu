@@ -301,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int g = 0;                      // blocks published
         uint32_t q_ph = 0;
+        bool q_issued = false;          // a query block was requested (lane 0)
+        uint32_t q_par = 0;             // the BQ_FULL phase of the last one
         for (;;) {
             const RowMsg m = next_row(p, lane, ok && !*sy.abort_flag);
             if (m.t < 0) break;
@@ -312,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive_expect_tx(bar(BQ_FULL), 8 * kQChunk);
                 for (int c = 0; c < 8; ++c)
                     ptx::tma_load_2d(sQ + c * kQChunk, &tm_q, bar(BQ_FULL), 64 * c, m.t * kH);
+                q_issued = true;
+                q_par = q_ph ^ 1;
             }
             for (int b = 0; b < nb && ok; ++b, ++g) {
                 int tk[4];
@@ -347,6 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && wait_bar_warp(bar(BI_EMPTY + is), ((g / kInfoSlots) & 1) ^ 1, sy) && lane == 0) {
             info[is].t = -1;
             ptx::mbar_arrive(bar(BI_FULL + is));
+        }
+        // no query-block load may still be in flight when the CTA ends (after an
+        // expired wait the MMA thread may not have taken the last one): a wait
+        // of its own, bounded by the default limit and blind to the abort flag
+        if (lane == 0 && q_issued) {
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(bar(BQ_FULL), q_par))
+                if (ptx::globaltimer() - t0 > kTimeoutNs) break;
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
