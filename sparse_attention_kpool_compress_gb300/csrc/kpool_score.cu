@@ -512,10 +512,12 @@ __device__ void group_rank_store(float *cs, int *ci, int n, int pool_base, int w
 // Direct mode: the n scores of one query at their local pool positions
 // dq[0..n).  Writes the best k (ties to the lower pool index), or all n when
 // n <= k, to out_idx/out_score in ascending pool order and returns how many
-// it wrote.  One selection group: a radix search for the k-th key, then two
-// ordered passes (counts per warp, then ballot-ranked writes).
+// it wrote.  One selection group: the scores are turned into their orderable
+// keys in place once (dq is scratch afterwards), then a radix search for the
+// k-th key and two ordered passes (counts per warp, then ballot-ranked writes)
+// read the keys.
 template <int NW = kGroupWarps>
-__device__ int group_select_direct(const float *dq, int n, int k, int pool_base, int g, int gtid,
+__device__ int group_select_direct(float *dq, int n, int k, int pool_base, int g, int gtid,
                                    int *hist, int *gs, int32_t *out_idx, float *out_score)
 {
     const int lane = gtid & 31, gw = gtid >> 5;
@@ -527,10 +529,13 @@ __device__ int group_select_direct(const float *dq, int n, int k, int pool_base,
         }
         return n;
     }
+    uint32_t *dk = reinterpret_cast<uint32_t *>(dq);
+    for (int e = gtid; e < n; e += (32 * NW)) dk[e] = fkey(dq[e]);
+    sel_bar<NW>(g);
     uint32_t kth;
     int above, inbin;
     bool edge;
-    radix_kth<NW>(n, k, [&](int e) { return fkey(dq[e]); }, [](int) { return true; }, false, 0, g,
+    radix_kth<NW>(n, k, [&](int e) { return dk[e]; }, [](int) { return true; }, false, 0, g,
               gtid, hist, gs, kth, above, inbin, edge);
     // edge: the bin holds exactly the entries still needed -> keep key >= kth;
     // otherwise keep key > kth and the first `need` entries equal to it
@@ -541,7 +546,7 @@ __device__ int group_select_direct(const float *dq, int n, int k, int pool_base,
     int cgt = 0, ceq = 0;
     for (int c = r0; c < r1; c += 32) {
         const int e = c + lane;
-        const uint32_t key = e < r1 ? fkey(dq[e]) : 0u;
+        const uint32_t key = e < r1 ? dk[e] : 0u;
         cgt += __popc(__ballot_sync(kFull, e < r1 && (edge ? key >= kth : key > kth)));
         ceq += __popc(__ballot_sync(kFull, e < r1 && !edge && key == kth));
     }
@@ -559,8 +564,7 @@ __device__ int group_select_direct(const float *dq, int n, int k, int pool_base,
     int eq_seen = base_eq;
     for (int c = r0; c < r1; c += 32) {
         const int e = c + lane;
-        const float v = e < r1 ? dq[e] : 0.f;
-        const uint32_t key = fkey(v);
+        const uint32_t key = e < r1 ? dk[e] : 0u;
         const bool gt = e < r1 && (edge ? key >= kth : key > kth);
         const bool eq = e < r1 && !edge && key == kth;
         const unsigned beq = __ballot_sync(kFull, eq);
@@ -569,7 +573,7 @@ __device__ int group_select_direct(const float *dq, int n, int k, int pool_base,
         if (keep) {
             const int d = pos + __popc(bk & lt);
             out_idx[d] = pool_base + e;
-            out_score[d] = v;
+            out_score[d] = __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
         }
         pos += __popc(bk);
         eq_seen += __popc(beq);
