@@ -178,6 +178,12 @@ __device__ __forceinline__ uint32_t fkey(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The score of an orderable key (fkey's inverse; -0 comes back as +0).
+__device__ __forceinline__ float unkey(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // The smallest score whose key exceeds k, so that fkey(s) > k exactly when
 // s >= pass_floor(k) for every score s (never NaN; -0 folded into +0): -inf
 // when every score passes, NaN when none does.  One float compare per pool
@@ -385,10 +391,15 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
 {
     const int lane = gtid & 31, gw = gtid >> 5;
     const unsigned lt = (1u << lane) - 1u;
+    // the scores become their orderable keys in place for the passes below, and
+    // the kept ones scores again at the end
+    uint32_t *ck = reinterpret_cast<uint32_t *>(cs);
+    for (int e = gtid; e < n; e += (32 * NW)) ck[e] = fkey(cs[e]);
+    sel_bar<NW>(g);
     uint32_t kth;
     int above, inbin;
     bool edge;
-    radix_kth<NW>(n, k, [&](int e) { return fkey(cs[e]); }, [](int) { return true; }, !exact, slack, g,
+    radix_kth<NW>(n, k, [&](int e) { return ck[e]; }, [](int) { return true; }, !exact, slack, g,
               gtid, hist, gs, kth, above, inbin, edge);
     // ties at the k-th score: keep the lowest pool indices among them
     uint32_t ithr = 0xFFFFFFFFu;   // keep tied entries with ci <= ithr
@@ -400,7 +411,7 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
         bool ied;
         sel_bar<NW>(g);   // gs reuse
         radix_kth<NW>(n, need, [&](int e) { return ~static_cast<uint32_t>(ci[e]); },
-                  [&](int e) { return fkey(cs[e]) == kth; }, false, 0, g, gtid, hist, gs, ik, iab,
+                  [&](int e) { return ck[e] == kth; }, false, 0, g, gtid, hist, gs, ik, iab,
                   iin, ied);
         ithr = ~ik;
     }
@@ -411,20 +422,19 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
     int cnt = 0;
     for (int c = r0; c < r1; c += 32) {
         const int e = c + lane;
-        float sv = 0.f;
+        uint32_t key = 0u;
         int iv = 0;
         bool keep = false;
         if (e < r1) {
-            sv = cs[e];
+            key = ck[e];
             iv = ci[e];
-            const uint32_t key = fkey(sv);
             keep = edge ? key >= kth
                         : (key > kth || (key == kth && static_cast<uint32_t>(iv) <= ithr));
         }
         const unsigned kb = __ballot_sync(kFull, keep);
         if (keep) {
             const int dst = r0 + cnt + __popc(kb & lt);
-            cs[dst] = sv;
+            ck[dst] = key;
             ci[dst] = iv;
         }
         cnt += __popc(kb);
@@ -442,21 +452,22 @@ __device__ int group_select(float *cs, int *ci, int n, int k, bool exact, int sl
         if (gw == w) {
             for (int c = 0; c < cnt; c += 32) {
                 const int i = c + lane;
-                float sv = 0.f;
+                uint32_t kv = 0u;
                 int iv = 0;
                 if (i < cnt) {
-                    sv = cs[r0 + i];
+                    kv = ck[r0 + i];
                     iv = ci[r0 + i];
                 }
                 __syncwarp();
                 if (i < cnt) {
-                    cs[mybase + i] = sv;
+                    ck[mybase + i] = kv;
                     ci[mybase + i] = iv;
                 }
             }
         }
         sel_bar<NW>(g);
     }
+    for (int e = gtid; e < total; e += (32 * NW)) cs[e] = unkey(ck[e]);
     if (gtid == 0) *thr_out = edge ? (kth > 0 ? kth - 1u : 0u) : kth;
     sel_bar<NW>(g);
     return total;
@@ -573,7 +584,7 @@ __device__ int group_select_direct(float *dq, int n, int k, int pool_base, int g
         if (keep) {
             const int d = pos + __popc(bk & lt);
             out_idx[d] = pool_base + e;
-            out_score[d] = __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+            out_score[d] = unkey(key);
         }
         pos += __popc(bk);
         eq_seen += __popc(beq);
