@@ -37,8 +37,9 @@
 // the block's output MMAs free the slots in order and the next block's rows
 // refill them while the remaining output MMAs run.  (Gathering every row twice,
 // into separate score and output rings so that the next block's scores could
-// overlap this block's softmax, measured slower: the gather rate, not the
-// MMAs, bounds this kernel.)  S^T is double-buffered in TMEM (2 x 64 columns)
+// overlap this block's softmax, measured slower: the second gather costs more
+// than the overlap gains.)  With one block in flight, a block's scores, softmax
+// and output follow one another.  S^T is double-buffered in TMEM (2 x 64 columns)
 // and O^T takes 4 x 64.  The online softmax keeps one reference maximum m per
 // head and rescales O^T in TMEM only when a block's score exceeds m by more
 // than 8 in the base-2 exponent; P = 2^(s*scale*log2(e) - m) <= 256 goes to
