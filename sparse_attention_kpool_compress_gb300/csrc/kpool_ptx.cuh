@@ -82,19 +82,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
-// Four rows (y0..y3) of one 2D tensor, x.. x+box-1 columns each, into four
-// consecutive box rows at dst (the tensor map's box is one row high).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *desc, uint32_t bar,
-                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
-                                            int32_t y3)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-        "l"(desc), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
-        : "memory");
-}
-
 // ---- tcgen05 ---------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
@@ -343,11 +330,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group()
-{
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all()
 {
